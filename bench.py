@@ -1,0 +1,554 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 TRSM library (L X = alpha B, left/lower/no-trans/
+non-unit, in place of B).
+
+Default workload ("square64"): m = n = 64, column-major, lda = ldb = 64,
+alpha = 1, strided batch of 4096 systems in each of f32, f64, complex64 and
+complex128 -- one step solves the four batches (four launches of the
+small-regime kernel).  Metric: GFLOPS counted as m^2 n real flops per system
+(x4 for complex), summed over the step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--large] [--nb-sweep] [--no-cpu-baseline]
+
+With N > 1 (torchrun, one rank per GPU) every rank solves its own batches
+(independent systems, no collective on the data path): weak scaling.
+
+--impl reference times the CPU oracle (plain forward substitution, f64
+accumulation, all host cores) on a bounded sample of the same workload.
+--large adds the blocked-path workloads (m = n = 16384 f32 / complex64 with
+the table's NB) to the JSON line under "detail".
+--nb-sweep times the blocked path for NB in {128, 256, 512} over m in
+{1024, 2048, 4096, 8192, 16384} and the four types, and prints the table.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import trsm_inputs as ti  # noqa: E402
+
+DTYPES = ("f32", "f64", "c64", "c128")
+TORCH_NAME = {"f32": "float32", "f64": "float64", "c64": "complex64", "c128": "complex128"}
+SQUARE = dict(m=64, n=64, batch=4096)
+FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
+FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike)
+SM_COUNT, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
+
+
+def fp32_alu_peak_tflops():
+    """FFMA peak from unit counts and the maximum SM clock: 152 SMs x 128
+    FP32 lanes x 2 flops x 2.07 GHz."""
+    return SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# --------------------------------------------------------------------------- ranks
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def reduce_max(dist, value, device=None):
+    """Max of a float over ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+def kernel_source_hash():
+    """Hash of the CUDA sources: ncu traffic figures are only valid for the
+    kernels they were captured on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "triangular_solve_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """dram bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def make_square_inputs(dtype, m, n, batch):
+    L, B = ti.generate(dtype, m, n, batch, kind="dd64")
+    return ti.to_storage(L, "col"), ti.to_storage(B, "col")
+
+
+# --------------------------------------------------------------------------- gb300 arm
+def run_gb300(args, ws, rank, local):
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+    tgb.build()
+    tg.load_library()
+    m, n, batch = SQUARE["m"], SQUARE["n"], SQUARE["batch"]
+    stream = torch.cuda.current_stream()
+
+    bufs = {}
+    for d in DTYPES:
+        a_np, b_np = make_square_inputs(d, m, n, batch)
+        bufs[d] = dict(
+            a=torch.from_numpy(a_np).to(dev),
+            b0=torch.from_numpy(b_np).to(dev),
+            b=torch.empty(b_np.shape, dtype=getattr(torch, TORCH_NAME[d]), device=dev),
+            a_host=torch.from_numpy(a_np).pin_memory(),
+            b_host=torch.from_numpy(b_np).pin_memory(),
+            out_host=torch.empty(b_np.shape, dtype=getattr(torch, TORCH_NAME[d])).pin_memory(),
+        )
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def solve(d):
+        bb = bufs[d]
+        tg.trsm_llnn_strided_batched(d, "col", m, n, 1.0, bb["a"], m, m * m, bb["b"], m, m * n, batch,
+                                     stream)
+
+    def step(evs=None):
+        for i, d in enumerate(DTYPES):
+            bufs[d]["b"].copy_(bufs[d]["b0"])
+            flush.fill_(i + 1)
+            if evs is not None:
+                evs[i][0].record(stream)
+            solve(d)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in DTYPES] for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            step(events[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(dist)
+    per_dtype_ms = {d: [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
+                    for i, d in enumerate(DTYPES)}
+    kernel_ms_total = sum(sum(v) for v in per_dtype_ms.values())
+    kernel_ms_max = reduce_max(dist, kernel_ms_total, dev)
+    step_flops = sum(ti.flops(d, m, n, batch) for d in DTYPES)
+    value = ws * step_flops * args.steps / (kernel_ms_max * 1e-3) / 1e9
+
+    # end to end through the public API: host buffers in pinned memory,
+    # copies inside the timed region
+    h2d = sum(bufs[d]["a_host"].numel() * bufs[d]["a_host"].element_size()
+              + bufs[d]["b_host"].numel() * bufs[d]["b_host"].element_size() for d in DTYPES)
+    d2h = sum(bufs[d]["out_host"].numel() * bufs[d]["out_host"].element_size() for d in DTYPES)
+
+    def e2e_step():
+        for d in DTYPES:
+            bb = bufs[d]
+            bb["a"].copy_(bb["a_host"], non_blocking=True)
+            bb["b"].copy_(bb["b_host"], non_blocking=True)
+            solve(d)
+            bb["out_host"].copy_(bb["b"], non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_wall = reduce_max(dist, time.perf_counter() - t0, dev)
+    barrier(dist)
+    e2e_value = ws * step_flops * e2e_steps / e2e_wall / 1e9
+
+    # parity spot check of the last e2e result against the oracle on rank 0
+    detail = {}
+    for d in DTYPES:
+        ms = statistics.mean(per_dtype_ms[d])
+        detail[d] = {
+            "ms_per_launch": round(ms, 5),
+            "gflops": round(ti.flops(d, m, n, batch) / (ms * 1e-3) / 1e9, 2),
+            "gbs": round(ti.algorithmic_bytes(d, m, n, batch) / (ms * 1e-3) / 1e9, 1),
+        }
+    # batch-1 latency (one system per launch), the pages' small-regime figure
+    for d in DTYPES:
+        a1, b1 = bufs[d]["a"][: m * m], bufs[d]["b"][: m * n]
+        for _ in range(5):
+            tg.trsm_llnn(d, m, n, 1.0, a1, m, b1, m, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        reps = 200
+        for _ in range(reps):
+            tg.trsm_llnn(d, m, n, 1.0, a1, m, b1, m, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        detail[d]["batch1_us"] = round(us, 2)
+        detail[d]["batch1_gflops"] = round(ti.flops(d, m, n, 1) / (us * 1e-6) / 1e9, 2)
+
+    peaks, peak_src = measured_peaks()
+    dom = max(DTYPES, key=lambda d: statistics.mean(per_dtype_ms[d]))
+    dom_ms = statistics.mean(per_dtype_ms[dom])
+    if dom in ("f64", "c128"):
+        roof = {"bound": "alu", "achieved": ti.flops(dom, m, n, batch) / (dom_ms * 1e-3) / 1e12,
+                "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "peak_source": "nominal GB300 FP64 rate (recipe table)"}
+    else:
+        roof = {"bound": "hbm", "achieved": ti.algorithmic_bytes(dom, m, n, batch) / (dom_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"hbm_gbs ({peak_src})"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = f"small_colreg_kernel<{dom}, 64> (square64 batch 4096)"
+    roof["traffic"] = recorded_traffic(f"small_colreg/{dom}/square64x4096")
+    roof["achieved"] = round(roof["achieved"], 3)
+    roof["frac"] = round(roof["frac"], 4)
+
+    out = {
+        "metric": "TRSM GFLOPS (m^2 n real flops, x4 complex), m=n=64 strided batch 4096, "
+                  "f32+f64+c64+c128 per step",
+        "value": round(value, 2), "unit": "GFLOPS", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(kernel_ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64+c64+c128",
+        "data": "synthetic (seeded: L strictly lower U(-1,1)/64, diag 1+U(0,1); B U(-1,1))",
+        "config": {"workload": "square64: m=n=64 column-major lda=ldb=64 alpha=1, strided batch 4096 "
+                               "per type, one launch per type", "m": m, "n": n, "batch_per_gpu": batch,
+                   "l2": "flushed (256 MB write) before every timed launch; B restored from a pristine copy",
+                   "parallelism": f"independent batches per GPU x{ws}"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GFLOPS", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": len(DTYPES) * args.steps,
+        "roofline": roof,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(wall, 4),
+        "detail": detail,
+    }
+    if args.large and rank == 0:
+        out["detail"]["large"] = run_large(torch, tg, dev, stream, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_large(torch, tg, dev, stream, peaks, reps=2):
+    """Blocked-path workloads: m = n = 16384 in f32 and complex64 (table NB)."""
+    res = {}
+    for d in ("f32", "c64"):
+        mm = 16384
+        L, B = ti.generate(d, mm, mm, 1, kind="ddm")
+        a = torch.from_numpy(ti.to_storage(L, "col")).to(dev)
+        b0 = torch.from_numpy(ti.to_storage(B, "col")).to(dev)
+        del L, B
+        b = torch.empty_like(b0)
+        nb = tg.trsm_llnn_select_nb(d, mm, mm)
+        wsb = tg.trsm_llnn_workspace_bytes(d, mm, mm, nb)
+        wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        b.copy_(b0)
+        tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)  # warm-up
+        times, phases = [], []
+        for _ in range(reps):
+            b.copy_(b0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        b.copy_(b0)
+        phases = tg.trsm_llnn_profile(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+        ms = statistics.mean(times)
+        gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
+        tot = sum(phases)
+        res[f"{d}_m{mm}"] = {
+            "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1),
+            "frac_of_fp32_alu_peak": round(gf / 1e3 / fp32_alu_peak_tflops(), 4),
+            "phase_share": {"diag_inversion": round(phases[0] / tot, 4),
+                            "block_apply": round(phases[1] / tot, 4),
+                            "gemm_update": round(phases[2] / tot, 4)},
+        }
+        del a, b0, b, wsp
+        torch.cuda.empty_cache()
+    return res
+
+
+def nb_sweep(args):
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    rows = []
+    for d in args.sweep_dtypes.split(","):
+        for mm in [int(x) for x in args.sweep_ms.split(",")]:
+            g = torch.Generator(device=dev).manual_seed(0)
+            t = getattr(torch, TORCH_NAME[d])
+            real_t = torch.float32 if d in ("f32", "c64") else torch.float64
+            # device-side synthetic inputs of the same distribution (timing only)
+            shape = (mm, mm)
+            if d in ("c64", "c128"):
+                lv = torch.complex(torch.rand(shape, generator=g, device=dev, dtype=real_t),
+                                   torch.rand(shape, generator=g, device=dev, dtype=real_t))
+                bv = torch.complex(torch.rand(shape, generator=g, device=dev, dtype=real_t),
+                                   torch.rand(shape, generator=g, device=dev, dtype=real_t)) * 2 - (1 + 1j)
+            else:
+                lv = torch.rand(shape, generator=g, device=dev, dtype=real_t)
+                bv = torch.rand(shape, generator=g, device=dev, dtype=real_t) * 2 - 1
+            lv = (lv * 2 - 1) / mm
+            lv.diagonal().copy_(1 + torch.rand(mm, generator=g, device=dev, dtype=real_t))
+            a = lv.to(t).t().contiguous().t()  # column-major
+            b0 = bv.to(t).t().contiguous().t()
+            del lv, bv
+            best = None
+            for nb in (128, 256, 512):
+                wsb = tg.trsm_llnn_workspace_bytes(d, mm, mm, nb)
+                wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+                b = b0.clone()
+                tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+                ts = []
+                for _ in range(args.sweep_reps):
+                    b.copy_(b0)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                ms = statistics.mean(ts)
+                gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
+                rows.append({"dtype": d, "m": mm, "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1)})
+                print(json.dumps(rows[-1]), flush=True)
+                if best is None or gf > best[1]:
+                    best = (nb, gf)
+                del wsp, b
+            rows.append({"dtype": d, "m": mm, "best_nb": best[0]})
+            print(json.dumps(rows[-1]), flush=True)
+            del a, b0
+            torch.cuda.empty_cache()
+    return rows
+
+
+# --------------------------------------------------------------------------- oracle arm
+def cpu_baseline(seconds=15.0):
+    """The oracle, as it stands, on the host cores: square64 systems of the
+    four types, a bounded sample of each batch, repeated for ~`seconds`."""
+    import oracle
+    oracle.build()
+    m, n = SQUARE["m"], SQUARE["n"]
+    sample = 512
+    data = {}
+    for d in DTYPES:
+        a, b = make_square_inputs(d, m, n, SQUARE["batch"])
+        data[d] = (a[: sample * m * m].copy(), b[: sample * m * n].copy())
+    flops_rep = sum(ti.flops(d, m, n, sample) for d in DTYPES)
+
+    def rep():
+        for d in DTYPES:
+            a, b = data[d]
+            bb = b.copy()
+            oracle.trsm_llnn(d, m, n, 1.0, a, m, bb, m, stride_a=m * m, stride_b=m * n, batch=sample)
+
+    rep()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        rep()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(flops_rep * reps / el / 1e9, 3), "unit": "GFLOPS", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{sample} of the 4096 systems per type (m=n=64, four types), x{reps} repetitions, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    m, n = SQUARE["m"], SQUARE["n"]
+    sample = 256
+    data = {}
+    for d in DTYPES:
+        a, b = make_square_inputs(d, m, n, SQUARE["batch"])
+        data[d] = (a[: sample * m * m].copy(), b[: sample * m * n].copy())
+
+    def step():
+        for d in DTYPES:
+            a, b = data[d]
+            bb = b.copy()
+            oracle.trsm_llnn(d, m, n, 1.0, a, m, bb, m, stride_a=m * m, stride_b=m * n, batch=sample)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    step_flops = sum(ti.flops(d, m, n, sample) for d in DTYPES)
+    value = step_flops * args.steps / el / 1e9
+    cores = oracle.max_threads()
+    sample_txt = f"{sample} of the 4096 systems per type (m=n=64, four types) per step"
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "TRSM GFLOPS (m^2 n real flops, x4 complex), m=n=64 strided batch 4096, "
+                  "f32+f64+c64+c128 per step",
+        "value": round(value, 3), "unit": "GFLOPS", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 accumulation (f32+f64+c64+c128 storage)", "data": "synthetic",
+        "config": {"workload": "square64: m=n=64 column-major, batch sample per type", "sample": sample_txt},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample_txt},
+        "e2e": {"value": round(value, 3), "unit": "GFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--large", action="store_true")
+    ap.add_argument("--nb-sweep", action="store_true")
+    ap.add_argument("--sweep-dtypes", default="f32,f64,c64,c128")
+    ap.add_argument("--sweep-ms", default="1024,2048,4096,8192,16384")
+    ap.add_argument("--sweep-reps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if args.nb_sweep:
+        nb_sweep(args)
+        return
+    run_gb300(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

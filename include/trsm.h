@@ -1,0 +1,156 @@
+/*
+ * trsm.h -- C ABI of the GB300 (sm_103a) triangular-solve library
+ *           (libtrsm_gb300.so).
+ *
+ * One operation, in four element types:
+ *
+ *     solve  L * X = alpha * B  for X, overwriting B,
+ *
+ * where L is the lower triangle (diagonal included) of the square matrix A.
+ * The strictly upper triangle of A is never read.  The diagonal is not
+ * assumed to be one.  This is the left-side, lower-triangular,
+ * non-transposed, non-unit-diagonal TRSM studied in "Hierarchical Shared
+ * Memory-Aware Optimization for TRSM on GPU Platforms" (developinglight.com
+ * summary, opening paragraph and "One framework, several paths"), and the
+ * SOLVE_TRI operation of llama.cpp PR 17457 ("SOLVE_TRI CUDA kernel for small
+ * matrices"), which adds batching over independent systems.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - A and B are DEVICE pointers owned by the caller.  A is only read; B is
+ *    overwritten with X.  Element types: TRSM_F32 float, TRSM_F64 double,
+ *    TRSM_C64 interleaved {float re, im}, TRSM_C128 interleaved
+ *    {double re, im}.  A and B must be aligned to their element size.
+ *  - alpha is a HOST pointer to one value of the element type (one float,
+ *    one double, or two floats / two doubles for the complex types).
+ *  - Leading dimensions and batch strides count ELEMENTS, not bytes (the
+ *    reviewers of llama.cpp PR 17457 asked for strides in units of the
+ *    element type).  Column-major: element (i, j) sits at j*ld + i and
+ *    ld >= max(1, rows).  Row-major: at i*ld + j and ld >= max(1, cols).
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call is asynchronous and stream-ordered: it enqueues
+ *    kernels and returns; there is no host synchronisation inside.
+ *  - Quick returns: m == 0, n == 0 or batch == 0 returns TRSM_SUCCESS without
+ *    touching memory.  alpha == 0 sets B to zero without reading A (BLAS).
+ *  - A zero (or non-finite) diagonal entry is not an error: IEEE inf/NaN
+ *    propagate into X and the call still returns TRSM_SUCCESS (llama.cpp PR
+ *    17457 removed its division-by-zero guard because a zero pivot means the
+ *    data is already corrupt).
+ *  - Argument errors return a negative status -k, k the 1-based position of
+ *    the first invalid argument (LAPACK xerbla style), and launch nothing.
+ *    A CUDA error returns TRSM_ERR_CUDA_BASE + cudaError_t.
+ *  - Work runs entirely in this library's kernels on the current device;
+ *    there is no CPU fallback.
+ */
+#ifndef TRSM_GB300_H
+#define TRSM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TRSM_F32 = 0, TRSM_F64 = 1, TRSM_C64 = 2, TRSM_C128 = 3 } trsm_dtype_t;
+typedef enum { TRSM_COL_MAJOR = 0, TRSM_ROW_MAJOR = 1 } trsm_layout_t;
+
+#define TRSM_SUCCESS 0
+#define TRSM_ERR_WORKSPACE 900      /* caller workspace too small or misaligned */
+#define TRSM_ERR_CUDA_BASE 1000     /* TRSM_ERR_CUDA_BASE + cudaError_t */
+
+/*
+ * Single column-major system:  L X = alpha B,  A is m x m (lda >= max(1,m)),
+ * B is m x n (ldb >= max(1,m)).
+ *
+ * m <= 64 runs the small-regime shared-memory kernel (one launch).  Larger m
+ * runs the blocked path of "Hierarchical Shared Memory-Aware Optimization for
+ * TRSM on GPU Platforms" (diagonal-block inversion, then per block row an
+ * apply X_t = D_t^{-1} R_t and a trailing GEMM update), with the block size
+ * NB taken from the library's compile-time table.  The blocked path needs a
+ * device workspace of trsm_llnn_workspace_bytes(dtype, m, n, 0) bytes; this
+ * entry point allocates it with cudaMallocAsync on `stream` and frees it with
+ * cudaFreeAsync on the same stream.  Use trsm_llnn_ex to pass your own.
+ *
+ * Arguments: 1 dtype, 2 m, 3 n, 4 alpha, 5 A, 6 lda, 7 B, 8 ldb, 9 stream.
+ */
+int trsm_llnn(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
+              const void *A, int64_t lda, void *B, int64_t ldb, void *stream);
+
+/*
+ * `batch` independent systems; system b's A starts at A + b*strideA and its
+ * B at B + b*strideB (element strides; any value, including 0 for a shared
+ * A, is accepted for A; strideB must keep the B matrices disjoint).
+ * `layout` applies to both A and B.  This is the batched SOLVE_TRI of
+ * llama.cpp PR 17457 (its 4-D tensors flattened to one batch index).
+ *
+ * m <= 64: one launch of the small-regime kernel over the whole batch.
+ * m > 64: the blocked path runs system by system on `stream` (correct, not
+ * tuned for throughput), allocating its workspace as trsm_llnn does.
+ *
+ * Arguments: 1 dtype, 2 layout, 3 m, 4 n, 5 alpha, 6 A, 7 lda, 8 strideA,
+ * 9 B, 10 ldb, 11 strideB, 12 batch, 13 stream.
+ */
+int trsm_llnn_strided_batched(trsm_dtype_t dtype, trsm_layout_t layout, int64_t m, int64_t n,
+                              const void *alpha, const void *A, int64_t lda, int64_t strideA,
+                              void *B, int64_t ldb, int64_t strideB, int64_t batch,
+                              void *stream);
+
+/*
+ * Block size NB the blocked path uses for (dtype, m, n): the entry of the
+ * compile-time "size x type -> block size" table of the nearest tabulated m
+ * ("Hierarchical Shared Memory-Aware Optimization for TRSM on GPU
+ * Platforms", adaptive blocking: offline sweep, online nearest-match lookup).
+ * Returns 0 when m <= 64 (no blocking) and a negative status for invalid
+ * arguments (1 dtype, 2 m, 3 n).
+ */
+int trsm_llnn_select_nb(trsm_dtype_t dtype, int64_t m, int64_t n);
+
+/*
+ * Device workspace in bytes the blocked path needs for (dtype, m, n) with
+ * block size nb (nb == 0: the table's choice; otherwise one of 128, 256,
+ * 512).  0 when m <= 64.  Returns (size_t)-1 for invalid arguments.
+ * The workspace holds the inverted diagonal blocks D_t^{-1} (m x NB) and one
+ * NB x n panel of X.
+ */
+size_t trsm_llnn_workspace_bytes(trsm_dtype_t dtype, int64_t m, int64_t n, int64_t nb);
+
+/*
+ * trsm_llnn with an explicit block size and a caller-owned workspace.
+ * nb: 0 = table choice, else 128, 256 or 512 (ignored when m <= 64).
+ * workspace: device pointer, 256-byte aligned, at least
+ * trsm_llnn_workspace_bytes(dtype, m, n, nb) bytes (may be NULL when that is
+ * 0).  The call allocates nothing.  The workspace must not be used by
+ * another call until this call's work on `stream` has finished.
+ * Returns TRSM_ERR_WORKSPACE when the workspace is too small or misaligned.
+ *
+ * Arguments: 1 dtype, 2 m, 3 n, 4 alpha, 5 A, 6 lda, 7 B, 8 ldb, 9 nb,
+ * 10 workspace, 11 ws_bytes, 12 stream.
+ */
+int trsm_llnn_ex(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
+                 const void *A, int64_t lda, void *B, int64_t ldb, int64_t nb,
+                 void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * trsm_llnn_ex, additionally timing its phases with CUDA events on `stream`
+ * and SYNCHRONISING the stream before returning (a profiling entry, not for
+ * production use):  ms[0] diagonal-block inversion, ms[1] the block applies
+ * X_t = D_t^{-1} R_t, ms[2] the trailing GEMM updates, in milliseconds (the
+ * split reported in "Hierarchical Shared Memory-Aware Optimization for TRSM
+ * on GPU Platforms", Table 3).  For m <= 64 the whole solve is reported in
+ * ms[1] and the other two are 0.  ms must point to 3 host floats.
+ *
+ * Arguments: 1..12 as trsm_llnn_ex, 13 ms.
+ */
+int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
+                      const void *A, int64_t lda, void *B, int64_t ldb, int64_t nb,
+                      void *workspace, size_t ws_bytes, void *stream, float *ms);
+
+/* Static, human-readable text for a status code returned by this library. */
+const char *trsm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRSM_GB300_H */

@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads and exports every symbol include/trsm.h
+declares; host-only entry points and argument checking work without a GPU
+(no call here reaches a kernel launch)."""
+import ctypes
+
+import pytest
+
+import triangular_solve_gb300 as tg
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from triangular_solve_gb300 import build
+    build.build()
+    return tg.load_library()
+
+
+EXPECTED = {"trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_select_nb",
+            "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string"}
+
+
+def test_header_declares_the_boundary():
+    assert EXPECTED <= set(tg.declared_functions())
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in tg.declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_no_torch_types_in_the_header():
+    text = open(tg.HEADER).read()
+    assert "torch" not in text.lower().replace("torch.complex", "")
+    assert "extern \"C\"" in text
+
+
+def test_select_nb_table(lib):
+    assert tg.trsm_llnn_select_nb("f64", 64, 64) == 0
+    for d in tg.DTYPES:
+        for m in (65, 1000, 1024, 3000, 16384, 100000):
+            assert tg.trsm_llnn_select_nb(d, m, m) in (128, 256, 512)
+    with pytest.raises(tg.TrsmError):
+        tg.trsm_llnn_select_nb(9, 100, 100)
+
+
+def test_workspace_bytes(lib):
+    assert tg.trsm_llnn_workspace_bytes("f32", 64, 64) == 0
+    assert tg.trsm_llnn_workspace_bytes("f32", 1000, 0) == 0
+    # m = 1000, NB = 128: 8 blocks of 128 x 128 plus a 128 x 70 panel, 4 bytes
+    w = 8 * 128 * 128 * 4
+    x = 128 * 70 * 4
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 128) == r(w) + r(x)
+    assert tg.trsm_llnn_workspace_bytes("c128", 1000, 70, 512) == r(2 * 512 * 512 * 16) + r(512 * 70 * 16)
+    with pytest.raises(ValueError):
+        tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 100)
+
+
+def test_status_strings(lib):
+    assert tg.trsm_status_string(0) == "success"
+    assert "invalid argument" in tg.trsm_status_string(-3)
+    assert "workspace" in tg.trsm_status_string(tg.ERR_WORKSPACE)
+
+
+def _call(lib, *args):
+    return lib.trsm_llnn(*args)
+
+
+def test_argument_errors_report_position(lib):
+    one = ctypes.byref(ctypes.c_double(1.0))
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    assert lib.trsm_llnn(7, 4, 4, one, fake, 4, fake, 4, None) == -1
+    assert lib.trsm_llnn(1, -1, 4, one, fake, 4, fake, 4, None) == -2
+    assert lib.trsm_llnn(1, 4, -1, one, fake, 4, fake, 4, None) == -3
+    assert lib.trsm_llnn(1, 4, 4, None, fake, 4, fake, 4, None) == -4
+    assert lib.trsm_llnn(1, 4, 4, one, None, 4, fake, 4, None) == -5
+    assert lib.trsm_llnn(1, 4, 4, one, fake, 3, fake, 4, None) == -6
+    assert lib.trsm_llnn(1, 4, 4, one, fake, 4, None, 4, None) == -7
+    assert lib.trsm_llnn(1, 4, 4, one, fake, 4, fake, 3, None) == -8
+    assert lib.trsm_llnn(1, 4, 4, one, fake + 4, 4, fake, 4, None) == -5  # misaligned double
+    # quick returns touch nothing
+    assert lib.trsm_llnn(1, 0, 4, one, None, 1, None, 1, None) == 0
+    assert lib.trsm_llnn(1, 4, 0, one, None, 4, None, 4, None) == 0
+
+
+def test_batched_argument_errors(lib):
+    one = ctypes.byref(ctypes.c_float(1.0))
+    fake = 1 << 20
+    f = lib.trsm_llnn_strided_batched
+    assert f(0, 2, 4, 4, one, fake, 4, 16, fake, 4, 16, 2, None) == -2
+    assert f(0, 0, 4, 4, one, fake, 4, -1, fake, 4, 16, 2, None) == -8
+    assert f(0, 1, 4, 6, one, fake, 4, 16, fake, 5, 30, 2, None) == -10   # row-major ldb < n
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 4, 15, 2, None) == -11   # overlapping B
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 4, 16, -1, None) == -12
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 4, 16, 0, None) == 0
+
+
+def test_ex_rejects_bad_block_size_and_workspace(lib):
+    one = ctypes.byref(ctypes.c_double(1.0))
+    fake = 1 << 20
+    assert lib.trsm_llnn_ex(1, 200, 4, one, fake, 200, fake, 200, 100, fake, 1 << 30, None) == -9
+    assert lib.trsm_llnn_ex(1, 200, 4, one, fake, 200, fake, 200, 128, None, 0, None) == tg.ERR_WORKSPACE
+    assert lib.trsm_llnn_ex(1, 200, 4, one, fake, 200, fake, 200, 128, fake + 8, 1 << 30, None) == \
+        tg.ERR_WORKSPACE
+    assert lib.trsm_llnn_ex(1, 200, 4, one, fake, 200, fake, 200, 128, fake, 16, None) == tg.ERR_WORKSPACE
+
+
+def test_cpu_tensors_are_refused():
+    torch = pytest.importorskip("torch")
+    A = torch.eye(4, dtype=torch.float64)
+    B = torch.ones(4, 2, dtype=torch.float64)
+    with pytest.raises(ValueError):
+        tg.solve(A, B)

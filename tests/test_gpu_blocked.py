@@ -1,0 +1,135 @@
+"""GPU parity of the blocked path (m > 64: diagonal-block inversion, block
+apply, trailing GEMM update) against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import trsm_inputs as ti
+from gpu_util import (TOL, assert_padding_untouched, assert_parity, gpu_solve_buffers, logical,
+                      oracle_buffers, storage_pair)
+
+pytestmark = pytest.mark.gpu
+DTYPES = ["f32", "f64", "c64", "c128"]
+TORCH_T = {"f32": "float32", "f64": "float64", "c64": "complex64", "c128": "complex128"}
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    tg.load_library()
+    return dict(torch=torch, tg=tg, oracle=oracle_mod)
+
+
+def _ex_solve(env, dtype, L, B, alpha, nb, lda=None, ldb=None, cols=None):
+    """Column-major single system through trsm_llnn_ex with a torch workspace."""
+    torch, tg = env["torch"], env["tg"]
+    a, b, geo = storage_pair(L, B, lda=lda, ldb=ldb, nan_upper=L.shape[1] <= 4096)
+    m, n = geo["m"], geo["n"]
+    ws_bytes = tg.trsm_llnn_workspace_bytes(dtype, m, n, nb)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    tA = torch.from_numpy(a).cuda()
+    tB = torch.from_numpy(b).cuda()
+    tg.trsm_llnn_ex(dtype, m, n, alpha, tA, geo["lda"], tB, geo["ldb"], nb, ws, ws_bytes)
+    torch.cuda.synchronize()
+    raw = tB.cpu().numpy()
+    del tA, tB, ws
+    ref = oracle_buffers(dtype, a, b, geo, alpha, env["oracle"], cols=cols)
+    xg, xr = logical(raw, geo), logical(ref, geo)
+    if cols is not None:
+        xg, xr = xg[:, :, cols], xr[:, :, cols]
+    else:
+        assert_padding_untouched(raw, b, geo)
+    return xg, xr
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("nb", [128, 256, 512])
+@pytest.mark.parametrize("m,n", [(65, 3), (129, 40), (300, 17), (700, 130)])
+def test_ragged_blocked(env, dtype, nb, m, n):
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + n)
+    alpha = (1.5 - 0.5j) if ti.IS_COMPLEX[dtype] else 1.5
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, nb, lda=m + 5, ldb=m + 3)
+    assert_parity(dtype, xg, xr, f"{dtype} m={m} n={n} nb={nb}")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_default_entry_allocates_its_workspace(env, dtype):
+    L, B = ti.generate(dtype, 520, 33, 1, kind="ddm")
+    a, b, geo = storage_pair(L, B)
+    raw = gpu_solve_buffers(dtype, a, b, geo, 2.0, env["torch"], env["tg"], single=True)
+    ref = oracle_buffers(dtype, a, b, geo, 2.0, env["oracle"])
+    assert_parity(dtype, logical(raw, geo), logical(ref, geo), "trsm_llnn auto workspace")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "c128"])
+@pytest.mark.parametrize("layout", ["col", "row"])
+def test_batched_blocked(env, dtype, layout):
+    L, B = ti.generate(dtype, 150, 20, 3, kind="ddm")
+    a, b, geo = storage_pair(L, B, layout=layout, lda=151, ldb=(150 if layout == "col" else 20) + 1)
+    raw = gpu_solve_buffers(dtype, a, b, geo, 0.75, env["torch"], env["tg"])
+    ref = oracle_buffers(dtype, a, b, geo, 0.75, env["oracle"])
+    assert_padding_untouched(raw, b, geo)
+    assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"batched blocked {layout}")
+
+
+def test_inverse_blocks_times_diagonal_blocks_is_identity(env):
+    """The inverted diagonal blocks left in the workspace satisfy W_t D_t = I
+    (the identity-tile substitution and the blocked inverse formula)."""
+    torch, tg = env["torch"], env["tg"]
+    dtype, m, n, nb = "f64", 1000, 8, 256
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm")
+    a, b, geo = storage_pair(L, B)
+    ws_bytes = tg.trsm_llnn_workspace_bytes(dtype, m, n, nb)
+    ws = torch.zeros(ws_bytes // 8, dtype=torch.float64, device="cuda")
+    tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    tg.trsm_llnn_ex(dtype, m, n, 1.0, tA, m, tB, m, nb, ws, ws_bytes)
+    torch.cuda.synchronize()
+    W = ws.cpu().numpy()
+    for t in range((m + nb - 1) // nb):
+        r0, mb = t * nb, min(nb, m - t * nb)
+        Wt = W[t * nb * nb:(t + 1) * nb * nb].reshape(nb, nb).T[:mb, :mb]   # column-major block
+        Dt = L[0, r0:r0 + mb, r0:r0 + mb]
+        np.testing.assert_allclose(Wt @ Dt, np.eye(mb), atol=1e-13)
+        assert np.all(np.triu(Wt, 1) == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f64", "c128"])
+def test_profile_reports_the_three_phases(env, dtype):
+    torch, tg = env["torch"], env["tg"]
+    m = n = 1024
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm")
+    a, b, geo = storage_pair(L, B, nan_upper=False)
+    ws_bytes = tg.trsm_llnn_workspace_bytes(dtype, m, n, 256)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ms = tg.trsm_llnn_profile(dtype, m, n, 1.5, tA, m, tB, m, 256, ws, ws_bytes)
+    assert all(v > 0 for v in ms)
+    ref = oracle_buffers(dtype, a, b, geo, 1.5, env["oracle"])
+    assert_parity(dtype, logical(tB.cpu().numpy(), geo), logical(ref, geo), "profile entry")
+
+
+# ------------------------------------------------------------- full workloads
+@pytest.mark.parametrize("dtype", ["f64", "c128"])
+@pytest.mark.parametrize("m", [1024, 2048, 8192])
+@pytest.mark.parametrize("nb", [128, 256, 512])
+def test_large_fp64_workload(env, dtype, m, nb):
+    """Square m = n, alpha = 1.5, L strictly lower U(-1,1)/m, diagonal 1 + U(0,1);
+    every NB of the sweep.  m >= 2048 is checked on the 64 sampled columns."""
+    L, B = ti.generate(dtype, m, m, 1, kind="ddm")
+    cols = ti.sample_columns(m) if m >= 2048 else None
+    xg, xr = _ex_solve(env, dtype, L, B, 1.5, nb, cols=cols)
+    assert_parity(dtype, xg, xr, f"{dtype} m={m} nb={nb}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
+def test_large_fp32_workload(env, dtype):
+    """Square m = n = 16384 with the table's NB, checked on the 64 sampled columns."""
+    m = 16384
+    L, B = ti.generate(dtype, m, m, 1, kind="ddm")
+    cols = ti.sample_columns(m)
+    xg, xr = _ex_solve(env, dtype, L, B, 1.0, 0, cols=cols)
+    assert_parity(dtype, xg, xr, f"{dtype} m={m}")

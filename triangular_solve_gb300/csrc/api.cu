@@ -1,0 +1,322 @@
+// C ABI of the GB300 triangular-solve library: argument checking, path
+// selection (small regime for m <= 64, blocked path above), workspace
+// handling and the row-major adapter.  See include/trsm.h for the contract.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "../../include/trsm.h"
+#include "blocked_kernels.cuh"
+#include "internal.h"
+#include "nb_table.h"
+
+using namespace trsm;
+
+namespace {
+
+int elem_bytes(int dtype) {
+    switch (dtype) {
+        case TRSM_F32: return 4;
+        case TRSM_F64: return 8;
+        case TRSM_C64: return 8;
+        case TRSM_C128: return 16;
+        default: return 0;
+    }
+}
+
+bool alpha_is_zero(int dtype, const void *alpha) {
+    switch (dtype) {
+        case TRSM_F32: return static_cast<const float *>(alpha)[0] == 0.f;
+        case TRSM_F64: return static_cast<const double *>(alpha)[0] == 0.0;
+        case TRSM_C64: {
+            const float *a = static_cast<const float *>(alpha);
+            return a[0] == 0.f && a[1] == 0.f;
+        }
+        default: {
+            const double *a = static_cast<const double *>(alpha);
+            return a[0] == 0.0 && a[1] == 0.0;
+        }
+    }
+}
+
+bool aligned(const void *p, int64_t a) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)a) == 0; }
+
+int64_t max1(int64_t x) { return x > 1 ? x : 1; }
+
+int nearest_nb(int dtype, int64_t m) {
+    int best = 0;
+    double best_d = 1e300;
+    for (const NbEntry &e : kNbTable) {
+        if (e.dtype != dtype) continue;
+        const double d = fabs(log2((double)m) - log2((double)e.m));
+        if (d < best_d) {
+            best_d = d;
+            best = e.nb;
+        }
+    }
+    return best ? best : 256;
+}
+
+int launch_small(int dtype, const SmallArgs &a, cudaStream_t st) {
+    if (a.n <= 8) {
+        switch (dtype) {
+            case TRSM_F32: return launch_rowlane_f32(a, st);
+            case TRSM_F64: return launch_rowlane_f64(a, st);
+            case TRSM_C64: return launch_rowlane_c64(a, st);
+            default: return launch_rowlane_c128(a, st);
+        }
+    }
+    switch (dtype) {
+        case TRSM_F32: return launch_colreg_f32(a, st);
+        case TRSM_F64: return launch_colreg_f64(a, st);
+        case TRSM_C64: return launch_colreg_c64(a, st);
+        default: return launch_colreg_c128(a, st);
+    }
+}
+
+int launch_zero(int dtype, const SmallArgs &a, cudaStream_t st) {
+    switch (dtype) {
+        case TRSM_F32: return launch_zero_f32(a, st);
+        case TRSM_F64: return launch_zero_f64(a, st);
+        case TRSM_C64: return launch_zero_c64(a, st);
+        default: return launch_zero_c128(a, st);
+    }
+}
+
+int blocked_solve(int dtype, const BlockedArgs &a, cudaStream_t st) {
+    switch (dtype) {
+        case TRSM_F32: return blocked_solve_f32(a, st);
+        case TRSM_F64: return blocked_solve_f64(a, st);
+        case TRSM_C64: return blocked_solve_c64(a, st);
+        default: return blocked_solve_c128(a, st);
+    }
+}
+
+// Everything after validation.  ws: caller workspace or NULL (then it is
+// allocated stream-ordered when the blocked path needs one).
+int solve(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda,
+          int64_t sA, void *B, int64_t ldb, int64_t sB, int64_t batch, int64_t nb, void *ws,
+          size_t ws_bytes, bool may_alloc, cudaStream_t st, float *ms) {
+    if (ms) ms[0] = ms[1] = ms[2] = 0.f;
+    if (m == 0 || n == 0 || batch == 0) return TRSM_SUCCESS;
+    SmallArgs s;
+    s.m = m; s.n = n; s.layout = layout;
+    s.A = A; s.lda = lda; s.strideA = sA;
+    s.B = B; s.ldb = ldb; s.strideB = sB;
+    s.batch = batch;
+    memset(s.alpha, 0, sizeof(s.alpha));
+    memcpy(s.alpha, alpha, (size_t)elem_bytes(dtype));
+    if (alpha_is_zero(dtype, alpha)) return launch_zero(dtype, s, st);
+
+    if (m <= 64) {
+        cudaEvent_t e0 = nullptr, e1 = nullptr;
+        if (ms) {
+            cudaEventCreate(&e0);
+            cudaEventCreate(&e1);
+            cudaEventRecord(e0, st);
+        }
+        int rc = launch_small(dtype, s, st);
+        if (ms) {
+            cudaEventRecord(e1, st);
+            cudaEventSynchronize(e1);
+            cudaEventElapsedTime(&ms[1], e0, e1);
+            cudaEventDestroy(e0);
+            cudaEventDestroy(e1);
+        }
+        return rc;
+    }
+
+    const int eb = elem_bytes(dtype);
+    if (nb == 0) nb = nearest_nb(dtype, m);
+    const size_t need = blocked_workspace_bytes(eb, m, n, nb);
+    // Row-major systems run through the column-major path on transposed
+    // copies held after the workspace.
+    const int64_t tl_bytes = layout == TRSM_ROW_MAJOR ? ((m * m * eb + 255) / 256) * 256 : 0;
+    const int64_t tb_bytes = layout == TRSM_ROW_MAJOR ? ((m * n * eb + 255) / 256) * 256 : 0;
+    const size_t total = need + (size_t)tl_bytes + (size_t)tb_bytes;
+    void *mem = ws;
+    bool owned = false;
+    if (mem == nullptr || ws_bytes < total) {
+        if (!may_alloc) return TRSM_ERR_WORKSPACE;
+        const cudaError_t e = cudaMallocAsync(&mem, total, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        owned = true;
+    }
+    int rc = TRSM_SUCCESS;
+    for (int64_t b = 0; b < batch && rc == TRSM_SUCCESS; ++b) {
+        BlockedArgs ba;
+        ba.m = m; ba.n = n; ba.nb = nb;
+        ba.ws = mem;
+        ba.ms = ms;
+        memcpy(ba.alpha, s.alpha, sizeof(ba.alpha));
+        const char *Ab = static_cast<const char *>(A) + b * sA * eb;
+        char *Bb = static_cast<char *>(B) + b * sB * eb;
+        if (layout == TRSM_COL_MAJOR) {
+            ba.A = Ab; ba.lda = lda;
+            ba.B = Bb; ba.ldb = ldb;
+            rc = blocked_solve(dtype, ba, st);
+        } else {
+            char *Lc = static_cast<char *>(mem) + need;
+            char *Bc = Lc + tl_bytes;
+            rc = launch_transpose_copy(eb, Ab, lda, Lc, m, m, m, st);
+            if (!rc) rc = launch_transpose_copy(eb, Bb, ldb, Bc, m, m, n, st);
+            ba.A = Lc; ba.lda = m;
+            ba.B = Bc; ba.ldb = m;
+            if (!rc) rc = blocked_solve(dtype, ba, st);
+            // back: column-major m x n (ld m) -> row-major (ld ldb) is the
+            // transpose copy of the n x m row-major view of Bc.
+            if (!rc) rc = launch_transpose_copy(eb, Bc, m, Bb, ldb, n, m, st);
+        }
+    }
+    if (owned) {
+        const cudaError_t e = cudaFreeAsync(mem, st);
+        if (rc == TRSM_SUCCESS && e != cudaSuccess) rc = cuda_status(e);
+    }
+    return rc;
+}
+
+}  // namespace
+
+namespace trsm {
+
+size_t blocked_workspace_bytes(int elem, int64_t m, int64_t n, int64_t nb) {
+    int64_t wb, xb;
+    const int64_t tb = (m + nb - 1) / nb;
+    wb = ((tb * nb * nb * elem + 255) / 256) * 256;
+    xb = ((nb * (n > 0 ? n : 1) * elem + 255) / 256) * 256;
+    return (size_t)(wb + xb);
+}
+
+template <typename T>
+static int transpose_typed(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
+                           int64_t cols, cudaStream_t st) {
+    const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+    transpose_kernel<T><<<grid, dim3(32, 8), 0, st>>>(static_cast<const T *>(src), ld_src, static_cast<T *>(dst),
+                                                      ld_dst, rows, cols);
+    return launch_status();
+}
+
+int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
+                          int64_t cols, cudaStream_t st) {
+    switch (elem_bytes) {
+        case 4: return transpose_typed<float>(src, ld_src, dst, ld_dst, rows, cols, st);
+        case 8: return transpose_typed<double>(src, ld_src, dst, ld_dst, rows, cols, st);
+        default: return transpose_typed<double2>(src, ld_src, dst, ld_dst, rows, cols, st);
+    }
+}
+
+}  // namespace trsm
+
+extern "C" {
+
+int trsm_llnn(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda, void *B,
+              int64_t ldb, void *stream) {
+    const int eb = elem_bytes(dtype);
+    if (!eb) return -1;
+    if (m < 0) return -2;
+    if (n < 0) return -3;
+    if (!alpha) return -4;
+    if (lda < max1(m)) return -6;
+    if (ldb < max1(m)) return -8;
+    if (m == 0 || n == 0) return TRSM_SUCCESS;
+    const bool zero = alpha_is_zero(dtype, alpha);
+    if (!zero && (!A || !aligned(A, eb))) return -5;
+    if (!B || !aligned(B, eb)) return -7;
+    if (m <= 64 && n > 64LL * 65535) return -3;
+    return solve(dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, 0, nullptr, 0, true,
+                 static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int trsm_llnn_strided_batched(trsm_dtype_t dtype, trsm_layout_t layout, int64_t m, int64_t n, const void *alpha,
+                              const void *A, int64_t lda, int64_t strideA, void *B, int64_t ldb, int64_t strideB,
+                              int64_t batch, void *stream) {
+    const int eb = elem_bytes(dtype);
+    if (!eb) return -1;
+    if (layout != TRSM_COL_MAJOR && layout != TRSM_ROW_MAJOR) return -2;
+    if (m < 0) return -3;
+    if (n < 0) return -4;
+    if (!alpha) return -5;
+    if (lda < max1(m)) return -7;
+    if (strideA < 0) return -8;
+    if (ldb < (layout == TRSM_COL_MAJOR ? max1(m) : max1(n))) return -10;
+    if (batch < 0) return -12;
+    if (batch > 1 && strideB < (layout == TRSM_COL_MAJOR ? ldb * n : ldb * m)) return -11;
+    if (m == 0 || n == 0 || batch == 0) return TRSM_SUCCESS;
+    const bool zero = alpha_is_zero(dtype, alpha);
+    if (!zero && (!A || !aligned(A, eb))) return -6;
+    if (!B || !aligned(B, eb)) return -9;
+    if (m <= 64 && n > 64LL * 65535) return -4;
+    return solve(dtype, layout, m, n, alpha, A, lda, strideA, B, ldb, strideB, batch, 0, nullptr, 0, true,
+                 static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int trsm_llnn_select_nb(trsm_dtype_t dtype, int64_t m, int64_t n) {
+    if (!elem_bytes(dtype)) return -1;
+    if (m < 0) return -2;
+    if (n < 0) return -3;
+    if (m <= 64) return 0;
+    return nearest_nb(dtype, m);
+}
+
+size_t trsm_llnn_workspace_bytes(trsm_dtype_t dtype, int64_t m, int64_t n, int64_t nb) {
+    const int eb = elem_bytes(dtype);
+    if (!eb || m < 0 || n < 0) return (size_t)-1;
+    if (nb != 0 && nb != 128 && nb != 256 && nb != 512) return (size_t)-1;
+    if (m <= 64 || n == 0) return 0;
+    if (nb == 0) nb = nearest_nb(dtype, m);
+    return blocked_workspace_bytes(eb, m, n, nb);
+}
+
+static int ex_common(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda,
+                     void *B, int64_t ldb, int64_t nb, void *workspace, size_t ws_bytes, void *stream, float *ms) {
+    const int eb = elem_bytes(dtype);
+    if (!eb) return -1;
+    if (m < 0) return -2;
+    if (n < 0) return -3;
+    if (!alpha) return -4;
+    if (lda < max1(m)) return -6;
+    if (ldb < max1(m)) return -8;
+    if (nb != 0 && nb != 128 && nb != 256 && nb != 512) return -9;
+    if (m == 0 || n == 0) {
+        if (ms) ms[0] = ms[1] = ms[2] = 0.f;
+        return TRSM_SUCCESS;
+    }
+    const bool zero = alpha_is_zero(dtype, alpha);
+    if (!zero && (!A || !aligned(A, eb))) return -5;
+    if (!B || !aligned(B, eb)) return -7;
+    if (m <= 64 && n > 64LL * 65535) return -3;
+    if (m > 64 && !zero) {
+        const size_t need = blocked_workspace_bytes(eb, m, n, nb ? nb : nearest_nb(dtype, m));
+        if (!workspace || !aligned(workspace, 256) || ws_bytes < need) return TRSM_ERR_WORKSPACE;
+    }
+    return solve(dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, nb, workspace, ws_bytes, false,
+                 static_cast<cudaStream_t>(stream), ms);
+}
+
+int trsm_llnn_ex(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda, void *B,
+                 int64_t ldb, int64_t nb, void *workspace, size_t ws_bytes, void *stream) {
+    return ex_common(dtype, m, n, alpha, A, lda, B, ldb, nb, workspace, ws_bytes, stream, nullptr);
+}
+
+int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda,
+                      void *B, int64_t ldb, int64_t nb, void *workspace, size_t ws_bytes, void *stream, float *ms) {
+    if (!ms) return -13;
+    const int rc = ex_common(dtype, m, n, alpha, A, lda, B, ldb, nb, workspace, ws_bytes, stream, ms);
+    if (rc == TRSM_SUCCESS) {
+        const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return rc;
+}
+
+const char *trsm_status_string(int status) {
+    if (status == TRSM_SUCCESS) return "success";
+    if (status < 0) return "invalid argument (the negated status is its 1-based position)";
+    if (status == TRSM_ERR_WORKSPACE) return "workspace missing, misaligned or too small";
+    if (status >= TRSM_ERR_CUDA_BASE) return cudaGetErrorString((cudaError_t)(status - TRSM_ERR_CUDA_BASE));
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,330 @@
+// Kernels of the blocked (m > 64) path.
+//
+// "Hierarchical Shared Memory-Aware Optimization for TRSM on GPU Platforms":
+// the lower triangle is split into block rows of NB; every diagonal block D_t
+// is inverted independently (different D_t go to different CTAs), each D_t
+// itself in I_B x I_B sub-blocks with I_B = NB/8.  The diagonal sub-blocks
+// are inverted by pure column-level substitution against identity tiles,
+// loading one column at a time into a double buffer (O(I_B) shared memory);
+// the inter-sub-block terms become matrix products through the blocked
+// triangular-inverse formula.  The solve then applies D_t^{-1} to the block
+// row and updates the trailing right-hand side with a GEMM, the dominant cost.
+#pragma once
+
+#include "common.cuh"
+#include "small_kernels.cuh"  // Vec, lds16, update_rows
+
+namespace trsm {
+
+// ---------------------------------------------------------------------------
+// Level 1: invert the diagonal I_B x I_B sub-block S of D_t.
+// CTA (t, i) handles S = L[r0 : r0+IB, r0 : r0+IB], r0 = t*NB + i*IB.
+// Thread j solves S y = e_j (column j of the identity tile) with y in
+// registers.  Column k of S is streamed through a two-slot shared buffer:
+// while slot k&1 feeds step k, slot (k+1)&1 receives column k+1 by cp.async.
+// Rows and columns at or beyond m are identity padding.
+// Output: the lower triangle of S^{-1} into W_t (NB x NB, column-major, ld
+// NB) at sub-block (i, i); the strictly upper sub-blocks (0..i-1, i) of
+// column block i are zero-filled.
+// ---------------------------------------------------------------------------
+template <typename T, int IB>
+__device__ __forceinline__ void inv_l1_prefetch(T *slot, const T *L, int64_t lda, int64_t m, int64_t r0, int k,
+                                                int tid) {
+    // rows 0..IB-1 of column k; thread tid loads row tid (IB threads)
+    const int64_t gr = r0 + tid, gc = r0 + k;
+    if (tid > k && gr < m) cp_async<sizeof(T)>(slot + tid, L + gc * lda + gr);
+    else if (tid == k) slot[tid] = (gr < m) ? ldg(L + gc * lda + gr) : T{};
+    else slot[tid] = zero_of<T>();
+}
+
+template <typename T> __device__ __forceinline__ T one_of();
+template <> __device__ __forceinline__ float one_of<float>() { return 1.f; }
+template <> __device__ __forceinline__ double one_of<double>() { return 1.0; }
+template <> __device__ __forceinline__ float2 one_of<float2>() { return make_float2(1.f, 0.f); }
+template <> __device__ __forceinline__ double2 one_of<double2>() { return make_double2(1.0, 0.0); }
+
+template <typename T, int IB, int K>
+struct InvL1Steps {
+    static __device__ __forceinline__ void run(T (&y)[IB], T (*buf)[IB], const T *L, int64_t lda, int64_t m,
+                                               int64_t r0, int tid) {
+        if constexpr (K < IB) {
+            if (K + 1 < IB) inv_l1_prefetch<T, IB>(buf[(K + 1) & 1], L, lda, m, r0, K + 1, tid);
+            cp_async_commit();
+            cp_async_wait<1>();
+            __syncthreads();
+            const T *col = buf[K & 1];
+            const T d = (r0 + K < m) ? col[K] : one_of<T>();
+            const T xk = mul(y[K], recip(d));
+            y[K] = xk;
+            update_rows<T, IB, K + 1>(col, xk, y);
+            __syncthreads();
+            InvL1Steps<T, IB, K + 1>::run(y, buf, L, lda, m, r0, tid);
+        }
+    }
+};
+
+template <typename T, int IB>
+__global__ void __launch_bounds__(IB) inv_diag_l1_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
+                                                         T *__restrict__ W) {
+    __shared__ __align__(16) T buf[2][IB];
+    const int t = blockIdx.x / 8, i = blockIdx.x % 8;
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)t * nb + (int64_t)i * IB;
+    T y[IB];
+#pragma unroll
+    for (int r = 0; r < IB; ++r) y[r] = (r == tid) ? one_of<T>() : zero_of<T>();
+    inv_l1_prefetch<T, IB>(buf[0], L, lda, m, r0, 0, tid);
+    cp_async_commit();
+    InvL1Steps<T, IB, 0>::run(y, buf, L, lda, m, r0, tid);
+    cp_async_wait_all();
+
+    T *Wt = W + (int64_t)t * nb * nb;
+    const int c = i * IB + tid;  // column of W_t owned by this thread
+    T *colp = Wt + (int64_t)c * nb;
+    for (int r = 0; r < i * IB; ++r) colp[r] = zero_of<T>();
+#pragma unroll
+    for (int r = 0; r < IB; ++r) colp[i * IB + r] = y[r];
+}
+
+// ---------------------------------------------------------------------------
+// Level 2: off-diagonal sub-blocks of W_t = D_t^{-1} along the wavefront
+// d = i - j (launched for d = 1..7 in order).  With S_ii the diagonal
+// sub-blocks and L_ik the sub-blocks of D_t,
+//     Y_ij = -Y_ii * sum_{k=j}^{i-1} L_ik Y_kj ,
+// every Y_kj on the right lying on an earlier wavefront.  CTA (t, j) forms
+// P = L[i-rows, j..i-1 cols] * Y[j..i-1 rows, j col] (K = d*IB) in shared
+// memory, then Y_ij = -Y_ii * P.  256 threads, each owning a TR x TC patch.
+// ---------------------------------------------------------------------------
+template <typename T, int IB>
+struct L2Cfg {
+    static constexpr int kThreads = 256;
+    static constexpr int kTR = IB >= 64 ? 4 : (IB >= 32 ? 2 : 1);
+    static constexpr int kTC = IB >= 64 ? 4 : (IB >= 32 ? 2 : 1);
+    static constexpr int kKC = 16;  // K chunk staged per step
+    static_assert((IB / kTR) * (IB / kTC) == kThreads, "level-2 thread tiling");
+};
+
+template <typename T, int IB>
+__global__ void __launch_bounds__(256) inv_offdiag_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
+                                                          T *__restrict__ W, int d) {
+    using C = L2Cfg<T, IB>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T *La = reinterpret_cast<T *>(smem_raw);  // [KC][IB]  (k-major chunk of L rows)
+    T *Yb = La + C::kKC * IB;                 // [KC][IB]  (k-major chunk of Y_kj)
+    T *P = Yb + C::kKC * IB;                  // [IB][IB + 1] column-major, padded
+    T *Yd = P + IB * (IB + 1);                // [IB][IB + 1] Y_ii column-major, padded
+    const int t = blockIdx.x, j = blockIdx.y, i = j + d;
+    const int tid = threadIdx.x;
+    const int tr = tid % (IB / C::kTR), tc = tid / (IB / C::kTR);
+    T *Wt = W + (int64_t)t * nb * nb;
+    const int64_t grow0 = (int64_t)t * nb + (int64_t)i * IB;   // global row of sub-block row i
+    const int64_t gcol0 = (int64_t)t * nb + (int64_t)j * IB;   // global col of sub-block col j
+    const int K = d * IB;
+
+    T acc[C::kTR][C::kTC];
+#pragma unroll
+    for (int a = 0; a < C::kTR; ++a)
+#pragma unroll
+        for (int b = 0; b < C::kTC; ++b) acc[a][b] = zero_of<T>();
+
+    for (int k0 = 0; k0 < K; k0 += C::kKC) {
+        __syncthreads();
+        for (int e = tid; e < C::kKC * IB; e += C::kThreads) {
+            const int kk = e / IB, r = e % IB;
+            const int64_t gr = grow0 + r, gc = gcol0 + k0 + kk;
+            La[kk * IB + r] = (gr < m) ? ldg(L + gc * lda + gr) : zero_of<T>();
+        }
+        for (int e = tid; e < C::kKC * IB; e += C::kThreads) {
+            const int kk = e % C::kKC, c = e / C::kKC;
+            // Y_kj rows j*IB + k0 + kk (contiguous in W_t), column j*IB + c
+            Yb[kk * IB + c] = Wt[(int64_t)(j * IB + c) * nb + (j * IB + k0 + kk)];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < C::kKC; ++kk) {
+            T a[C::kTR], b[C::kTC];
+#pragma unroll
+            for (int q = 0; q < C::kTR; ++q) a[q] = La[kk * IB + tr * C::kTR + q];
+#pragma unroll
+            for (int q = 0; q < C::kTC; ++q) b[q] = Yb[kk * IB + tc * C::kTC + q];
+#pragma unroll
+            for (int x = 0; x < C::kTR; ++x)
+#pragma unroll
+                for (int y = 0; y < C::kTC; ++y) acc[x][y] = fma_(a[x], b[y], acc[x][y]);
+        }
+    }
+    // P and Y_ii into shared memory
+#pragma unroll
+    for (int x = 0; x < C::kTR; ++x)
+#pragma unroll
+        for (int y = 0; y < C::kTC; ++y) P[(tc * C::kTC + y) * (IB + 1) + tr * C::kTR + x] = acc[x][y];
+    for (int e = tid; e < IB * IB; e += C::kThreads) {
+        const int c = e / IB, r = e % IB;
+        Yd[c * (IB + 1) + r] = Wt[(int64_t)(i * IB + c) * nb + (i * IB + r)];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < C::kTR; ++a)
+#pragma unroll
+        for (int b = 0; b < C::kTC; ++b) acc[a][b] = zero_of<T>();
+    for (int k = 0; k < IB; ++k) {
+        T a[C::kTR], b[C::kTC];
+#pragma unroll
+        for (int q = 0; q < C::kTR; ++q) a[q] = Yd[k * (IB + 1) + tr * C::kTR + q];
+#pragma unroll
+        for (int q = 0; q < C::kTC; ++q) b[q] = P[(tc * C::kTC + q) * (IB + 1) + k];
+#pragma unroll
+        for (int x = 0; x < C::kTR; ++x)
+#pragma unroll
+            for (int y = 0; y < C::kTC; ++y) acc[x][y] = fms(a[x], b[y], acc[x][y]);
+    }
+    // Y_ij into W_t rows i*IB.., cols j*IB..
+#pragma unroll
+    for (int y = 0; y < C::kTC; ++y) {
+        T *colp = Wt + (int64_t)(j * IB + tc * C::kTC + y) * nb + i * IB + tr * C::kTR;
+#pragma unroll
+        for (int x = 0; x < C::kTR; ++x) colp[x] = acc[x][y];
+    }
+}
+
+template <typename T, int IB>
+constexpr size_t inv_offdiag_smem() {
+    return sizeof(T) * (2 * L2Cfg<T, IB>::kKC * IB + 2 * IB * (IB + 1));
+}
+
+// ---------------------------------------------------------------------------
+// Tiled GEMM  C = beta*C + gamma * A * B  (all column-major; beta_zero skips
+// reading C).  With a_lower, A is lower triangular and the K loop of a
+// row tile stops at the tile's last row.  256 threads, a TM x TN register
+// patch per thread, double-buffered cp.async staging of BK-deep slabs.
+// ---------------------------------------------------------------------------
+template <typename T> struct GemmCfg;
+template <> struct GemmCfg<float>   { static constexpr int BM = 128, BN = 128, BK = 16, TM = 8, TN = 8; };
+template <> struct GemmCfg<double>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
+template <> struct GemmCfg<float2>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
+template <> struct GemmCfg<double2> { static constexpr int BM = 64,  BN = 32,  BK = 8,  TM = 4, TN = 2; };
+
+template <typename T>
+struct GemmArgs {
+    int64_t M, N, K;
+    const T *A;
+    int64_t lda;
+    const T *B;
+    int64_t ldb;
+    T *C;
+    int64_t ldc;
+    T gamma, beta;
+    int beta_zero, a_lower;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
+    using C = GemmCfg<T>;
+    constexpr int BM = C::BM, BN = C::BN, BK = C::BK, TM = C::TM, TN = C::TN;
+    constexpr int NT = (BM / TM) * (BN / TN);
+    static_assert(NT == 256, "gemm threads");
+    constexpr int BPAD = 16 / (int)sizeof(T) > 1 ? 16 / (int)sizeof(T) : 1;
+    __shared__ __align__(16) T As[2][BK][BM];
+    __shared__ __align__(16) T Bs[2][BK][BN + BPAD];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % (BM / TM), ty = tid / (BM / TM);
+    const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN;
+    int64_t kend = g.K;
+    if (g.a_lower && m0 + BM < kend) kend = m0 + BM;
+    const int nk = (int)((kend + BK - 1) / BK);
+
+    auto load = [&](int kt, int s) {
+        const int64_t k0 = (int64_t)kt * BK;
+        for (int e = tid; e < BM * BK; e += NT) {
+            const int kk = e / BM, r = e % BM;
+            const int64_t gr = m0 + r, gk = k0 + kk;
+            if (gr < g.M && gk < kend) cp_async<sizeof(T)>(&As[s][kk][r], g.A + gk * g.lda + gr);
+            else As[s][kk][r] = zero_of<T>();
+        }
+        for (int e = tid; e < BK * BN; e += NT) {
+            const int kk = e % BK, c = e / BK;
+            const int64_t gc = n0 + c, gk = k0 + kk;
+            if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gc * g.ldb + gk);
+            else Bs[s][kk][c] = zero_of<T>();
+        }
+    };
+
+    T acc[TM][TN];
+#pragma unroll
+    for (int a = 0; a < TM; ++a)
+#pragma unroll
+        for (int b = 0; b < TN; ++b) acc[a][b] = zero_of<T>();
+
+    if (nk > 0) load(0, 0);
+    cp_async_commit();
+    for (int kt = 0; kt < nk; ++kt) {
+        if (kt + 1 < nk) load(kt + 1, (kt + 1) & 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int s = kt & 1;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            T a[TM], b[TN];
+#pragma unroll
+            for (int q = 0; q < TM; ++q) a[q] = As[s][kk][tx * TM + q];
+#pragma unroll
+            for (int q = 0; q < TN; ++q) b[q] = Bs[s][kk][ty * TN + q];
+#pragma unroll
+            for (int x = 0; x < TM; ++x)
+#pragma unroll
+                for (int y = 0; y < TN; ++y) acc[x][y] = fma_(a[x], b[y], acc[x][y]);
+        }
+        __syncthreads();
+    }
+    cp_async_wait_all();
+
+#pragma unroll
+    for (int y = 0; y < TN; ++y) {
+        const int64_t gc = n0 + ty * TN + y;
+        if (gc >= g.N) continue;
+#pragma unroll
+        for (int x = 0; x < TM; ++x) {
+            const int64_t gr = m0 + tx * TM + x;
+            if (gr >= g.M) continue;
+            T *cp = g.C + gc * g.ldc + gr;
+            T v = mul(g.gamma, acc[x][y]);
+            if (!g.beta_zero) v = fma_(g.beta, *cp, v);
+            *cp = v;
+        }
+    }
+}
+
+// dst[r, c] = src[r, c] for an rows x cols column-major block.
+template <typename T>
+__global__ void copy_block_kernel(const T *__restrict__ src, int64_t lds, T *__restrict__ dst, int64_t ldd,
+                                  int64_t rows, int64_t cols) {
+    const int64_t total = rows * cols;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t c = e / rows, r = e - c * rows;
+        dst[c * ldd + r] = src[c * lds + r];
+    }
+}
+
+// dst (column-major rows x cols, ld_dst) = transpose-view of src, where src
+// holds the same logical matrix row-major (ld_src): dst[c*ld_dst + r] =
+// src[r*ld_src + c].  32 x 32 tiles through shared memory.
+template <typename T>
+__global__ void transpose_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst, int64_t ld_dst,
+                                 int64_t rows, int64_t cols) {
+    __shared__ T tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + q, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[q][threadIdx.x] = src[r * ld_src + c];
+    }
+    __syncthreads();
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t c = c0 + q, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) dst[c * ld_dst + r] = tile[threadIdx.x][q];
+    }
+}
+
+}  // namespace trsm

@@ -1,0 +1,65 @@
+// Internal interfaces between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace trsm {
+
+// One (strided-batched) solve, arguments already validated.  alpha holds one
+// value of the element type (up to two doubles).
+struct SmallArgs {
+    int64_t m, n;
+    int layout;  // 0 column-major, 1 row-major
+    const void *A;
+    int64_t lda, strideA;
+    void *B;
+    int64_t ldb, strideB;
+    int64_t batch;
+    alignas(16) unsigned char alpha[16];
+};
+
+// Small regime, m <= 64: one launch over the whole batch.  colreg: one
+// thread per RHS column (n > 8); rowlane: one warp per system (n <= 8).
+int launch_colreg_f32(const SmallArgs &a, cudaStream_t st);
+int launch_colreg_f64(const SmallArgs &a, cudaStream_t st);
+int launch_colreg_c64(const SmallArgs &a, cudaStream_t st);
+int launch_colreg_c128(const SmallArgs &a, cudaStream_t st);
+int launch_rowlane_f32(const SmallArgs &a, cudaStream_t st);
+int launch_rowlane_f64(const SmallArgs &a, cudaStream_t st);
+int launch_rowlane_c64(const SmallArgs &a, cudaStream_t st);
+int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st);
+
+// alpha == 0: B <- 0 without reading A.
+int launch_zero_f32(const SmallArgs &a, cudaStream_t st);
+int launch_zero_f64(const SmallArgs &a, cudaStream_t st);
+int launch_zero_c64(const SmallArgs &a, cudaStream_t st);
+int launch_zero_c128(const SmallArgs &a, cudaStream_t st);
+
+// Blocked path for one column-major system, m > 64.
+struct BlockedArgs {
+    int64_t m, n, nb;
+    const void *A;
+    int64_t lda;
+    void *B;
+    int64_t ldb;
+    alignas(16) unsigned char alpha[16];
+    void *ws;        // >= blocked_workspace_bytes(elem, m, n, nb), 256-byte aligned
+    float *ms;       // optional: per-phase milliseconds (profiling entry)
+};
+
+// Bytes of workspace the blocked path needs.
+size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb);
+
+int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);
+int blocked_solve_f64(const BlockedArgs &a, cudaStream_t st);
+int blocked_solve_c64(const BlockedArgs &a, cudaStream_t st);
+int blocked_solve_c128(const BlockedArgs &a, cudaStream_t st);
+
+// Row-major <-> column-major copy of a rows x cols matrix (out-of-place),
+// used to run row-major inputs through the column-major blocked path.
+int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, cudaStream_t st);
+
+}  // namespace trsm

@@ -1,0 +1,8 @@
+// Small-regime (m <= 64) thread-per-column launches for element type float2,
+// and the alpha == 0 fill.
+#include "small_launch.cuh"
+
+namespace trsm {
+int launch_colreg_c64(const SmallArgs &a, cudaStream_t st) { return launch_colreg_typed<float2>(a, st); }
+int launch_zero_c64(const SmallArgs &a, cudaStream_t st) { return launch_zero_typed<float2>(a, st); }
+}  // namespace trsm

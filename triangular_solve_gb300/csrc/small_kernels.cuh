@@ -1,0 +1,311 @@
+// Small-regime TRSM kernels (m <= 64): the whole lower triangle of one
+// system and its right-hand-side slice are staged on chip, then solved by
+// forward substitution without touching global memory again.
+//
+// "Hierarchical Shared Memory-Aware Optimization for TRSM on GPU Platforms",
+// small-scale regime (m, n <= 64): A is held entirely in shared memory and the
+// right-hand side is staged on chip, with the solve overlapped with memory
+// traffic.  The pages size this for a 48-64 KB budget (half of B at a time,
+// and a seven-stage two-group pipeline for complex double).  On sm_103a a CTA
+// may use up to 227 KB, so every type -- complex double included -- stages
+// the full lower triangle and the full RHS slice at once, and the overlap
+// comes from several CTAs per SM instead of an intra-CTA pipeline.
+//
+// Two thread mappings:
+//  * colreg  (n > 8):  one thread per RHS column.  The thread keeps its
+//    column in registers (in row chunks of RC for wide types) and walks the
+//    columns of L left to right (x_k = b_k / L_kk, then b_i -= L_ik x_k for
+//    i > k).  Every thread of a system reads the same L_ik, so the shared
+//    loads are broadcasts and there is no per-row reduction or barrier (the
+//    llama.cpp SOLVE_TRI kernel of PR 17457 instead reduces a dot product
+//    across a warp and synchronises after every row).
+//  * rowlane (n <= 8): one warp per system, lane l owns rows l and l+32 of
+//    every column; x_k travels from its owner lane by a register shuffle.
+#pragma once
+
+#include "common.cuh"
+
+namespace trsm {
+
+struct SmallGeom {
+    int m, n, layout;  // layout: 0 column-major, 1 row-major
+    const void *A;
+    int64_t lda, sA;
+    void *B;
+    int64_t ldb, sB;
+    int64_t batch;
+    int spc;  // systems per CTA
+    int w;    // RHS columns per CTA slice (colreg) / register columns (rowlane)
+};
+
+// Shared-memory image of one system:
+//   Ls   M x M, column-major (ld M): the strictly lower part of L; the
+//        diagonal and everything above it hold zero.
+//   dinv M reciprocals of the diagonal (zero for padding rows >= m).
+//   Bs   w columns of the RHS, column stride M + 1 (odd, so a thread per
+//        column reads its own column without bank conflicts).
+template <typename T, int M>
+struct SmallImage {
+    static constexpr int kBld = M + 1;
+    static __host__ __device__ __forceinline__ int elems(int w) {
+        const int e = M * M + M + w * kBld;
+        constexpr int a = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T);
+        return (e + a - 1) / a * a;  // keep every system's Ls 16-byte aligned
+    }
+};
+
+// Cooperative copy of system `sys` into its shared image.  Elements copied
+// from memory go through cp.async; the complement is zero-filled with plain
+// stores (disjoint addresses, so no ordering is needed between the two).
+template <typename T, int M>
+__device__ __forceinline__ void stage_system(const SmallGeom &g, T *Ls, T *dinv, T *Bs, int64_t sys,
+                                             int j0, int wcols, int tid, int nthr) {
+    const T *A = static_cast<const T *>(g.A) + sys * g.sA;
+    const T *B = static_cast<const T *>(g.B) + sys * g.sB;
+    const int m = g.m;
+    const T z = zero_of<T>();
+    if (g.layout == 0) {
+        for (int e = tid; e < M * M; e += nthr) {
+            const int k = e / M, i = e - k * M;
+            if (i > k && i < m) cp_async<sizeof(T)>(Ls + e, A + (int64_t)k * g.lda + i);
+            else Ls[e] = z;
+        }
+        for (int e = tid; e < wcols * M; e += nthr) {
+            const int c = e / M, i = e - c * M;
+            T *d = Bs + c * (M + 1) + i;
+            if (i < m) cp_async<sizeof(T)>(d, B + (int64_t)(j0 + c) * g.ldb + i);
+            else *d = z;
+        }
+    } else {
+        for (int e = tid; e < M * M; e += nthr) {
+            const int i = e / M, k = e - i * M;
+            if (i > k && i < m) cp_async<sizeof(T)>(Ls + k * M + i, A + (int64_t)i * g.lda + k);
+            else Ls[k * M + i] = z;
+        }
+        for (int e = tid; e < wcols * M; e += nthr) {
+            const int i = e / wcols, c = e - i * wcols;
+            T *d = Bs + c * (M + 1) + i;
+            if (i < m) cp_async<sizeof(T)>(d, B + (int64_t)i * g.ldb + (j0 + c));
+            else *d = z;
+        }
+    }
+    for (int e = tid; e < M; e += nthr) dinv[e] = e < m ? recip(ldg(A + (int64_t)e * g.lda + e)) : z;
+}
+
+template <typename T, int M>
+__device__ __forceinline__ void unstage_system(const SmallGeom &g, const T *Bs, int64_t sys, int j0,
+                                               int wcols, int tid, int nthr) {
+    T *B = static_cast<T *>(g.B) + sys * g.sB;
+    const int m = g.m;
+    if (g.layout == 0) {
+        for (int e = tid; e < wcols * M; e += nthr) {
+            const int c = e / M, i = e - c * M;
+            if (i < m) B[(int64_t)(j0 + c) * g.ldb + i] = Bs[c * (M + 1) + i];
+        }
+    } else {
+        for (int e = tid; e < wcols * M; e += nthr) {
+            const int i = e / wcols, c = e - i * wcols;
+            if (i < m) B[(int64_t)i * g.ldb + (j0 + c)] = Bs[c * (M + 1) + i];
+        }
+    }
+}
+
+// Vector width (elements per 16-byte shared load).
+template <typename T> struct Vec { static constexpr int kN = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T); };
+
+template <typename T>
+__device__ __forceinline__ void lds16(const T *p, T (&out)[Vec<T>::kN]) {
+    if constexpr (Vec<T>::kN == 1) {
+        out[0] = *p;
+    } else {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        const T *s = reinterpret_cast<const T *>(&v);
+#pragma unroll
+        for (int q = 0; q < Vec<T>::kN; ++q) out[q] = s[q];
+    }
+}
+
+// b[ii] -= col[ii] * xk for ii in [FROM, RC).  col is 16-byte aligned; rows
+// are read in 16-byte broadcast loads where a whole group is in range.
+template <typename T, int RC, int FROM>
+__device__ __forceinline__ void update_rows(const T *__restrict__ col, const T xk, T (&b)[RC]) {
+    constexpr int V = Vec<T>::kN;
+#pragma unroll
+    for (int g0 = 0; g0 < RC; g0 += V) {
+        if (g0 + V <= FROM) continue;
+        if (g0 >= FROM && g0 + V <= RC) {
+            T l[V];
+            lds16<T>(col + g0, l);
+#pragma unroll
+            for (int v = 0; v < V; ++v) b[g0 + v] = fms(l[v], xk, b[g0 + v]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (g0 + v >= FROM && g0 + v < RC) b[g0 + v] = fms(col[g0 + v], xk, b[g0 + v]);
+        }
+    }
+}
+
+// Diagonal-block step kk of a chunk, recursing at compile time so that the
+// row range of every update is a constant.
+template <typename T, int M, int RC, int CH, int KK>
+struct DiagSteps {
+    static __device__ __forceinline__ void run(const T *__restrict__ Ls, const T *__restrict__ dinv, T (&b)[RC]) {
+        if constexpr (KK < RC) {
+            constexpr int k = CH * RC + KK;
+            const T xk = mul(b[KK], dinv[k]);
+            b[KK] = xk;
+            update_rows<T, RC, KK + 1>(Ls + k * M + CH * RC, xk, b);
+            DiagSteps<T, M, RC, CH, KK + 1>::run(Ls, dinv, b);
+        }
+    }
+};
+
+// Solve one column (staged at bs, stride 1) in chunks of RC rows; solved
+// chunks are written back to bs, from where later chunks read them.
+template <typename T, int M, int RC, int CH>
+struct ColumnChunks {
+    static __device__ __forceinline__ void run(const T *__restrict__ Ls, const T *__restrict__ dinv, T *bs,
+                                               const T alpha) {
+        if constexpr (CH < M / RC) {
+            T b[RC];
+#pragma unroll
+            for (int ii = 0; ii < RC; ++ii) b[ii] = mul(alpha, bs[CH * RC + ii]);
+#pragma unroll
+            for (int k = 0; k < CH * RC; ++k) {
+                const T xk = bs[k];
+                update_rows<T, RC, 0>(Ls + k * M + CH * RC, xk, b);
+            }
+            DiagSteps<T, M, RC, CH, 0>::run(Ls, dinv, b);
+#pragma unroll
+            for (int ii = 0; ii < RC; ++ii) bs[CH * RC + ii] = b[ii];
+            ColumnChunks<T, M, RC, CH + 1>::run(Ls, dinv, bs, alpha);
+        }
+    }
+};
+
+template <typename T, int M, int RC>
+__global__ void __launch_bounds__(256) small_colreg_kernel(const SmallGeom g, const T alpha) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T *base = reinterpret_cast<T *>(smem_raw);
+    const int w = g.w;
+    const int per = SmallImage<T, M>::elems(w);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int j0 = blockIdx.y * w;
+    const int wcols = min(w, g.n - j0);
+    const int64_t sys0 = (int64_t)blockIdx.x * g.spc;
+    const int nsys = (int)min((int64_t)g.spc, g.batch - sys0);
+
+    for (int s = 0; s < nsys; ++s) {
+        T *Ls = base + s * per;
+        stage_system<T, M>(g, Ls, Ls + M * M, Ls + M * M + M, sys0 + s, j0, wcols, tid, nthr);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    const int s = tid / w, c = tid - s * w;
+    if (s < nsys && c < wcols) {
+        const T *Ls = base + s * per;
+        T *bs = base + s * per + M * M + M + c * (M + 1);
+        ColumnChunks<T, M, RC, 0>::run(Ls, Ls + M * M, bs, alpha);
+    }
+    __syncthreads();
+
+    for (int q = 0; q < nsys; ++q)
+        unstage_system<T, M>(g, base + q * per + M * M + M, sys0 + q, j0, wcols, tid, nthr);
+}
+
+// ---------------------------------------------------------------- rowlane
+__device__ __forceinline__ float shfl(float v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+__device__ __forceinline__ double shfl(double v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+__device__ __forceinline__ float2 shfl(float2 v, int src) {
+    return make_float2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+}
+__device__ __forceinline__ double2 shfl(double2 v, int src) {
+    return make_double2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+}
+
+template <typename T, int M, int NC>
+__global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, const T alpha) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int S = (M + 31) / 32;  // row slots per lane
+    T *base = reinterpret_cast<T *>(smem_raw);
+    const int per = SmallImage<T, M>::elems(NC);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n = g.n;
+    const int64_t sys0 = (int64_t)blockIdx.x * g.spc;
+    const int nsys = (int)min((int64_t)g.spc, g.batch - sys0);
+
+    for (int s = 0; s < nsys; ++s) {
+        T *Ls = base + s * per;
+        stage_system<T, M>(g, Ls, Ls + M * M, Ls + M * M + M, sys0 + s, 0, n, tid, nthr);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    if (warp < nsys) {  // warp-uniform
+        const T *Ls = base + warp * per;
+        const T *dinv = Ls + M * M;
+        T *Bs = base + warp * per + M * M + M;
+        T b[S][NC];
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            const int i = lane + 32 * s2;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+                b[s2][c] = (i < M && c < n) ? mul(alpha, Bs[c * (M + 1) + i]) : zero_of<T>();
+        }
+#pragma unroll
+        for (int k = 0; k < M; ++k) {
+            const int owner = k & 31, slot = k >> 5;
+            const T d = dinv[k];
+            T x[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) x[c] = mul(shfl(b[slot][c], owner), d);
+            if (lane == owner) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) b[slot][c] = x[c];
+            }
+#pragma unroll
+            for (int s2 = slot; s2 < S; ++s2) {
+                const int i = lane + 32 * s2;
+                if (i > k && i < M) {
+                    const T l = Ls[k * M + i];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) b[s2][c] = fms(l, x[c], b[s2][c]);
+                }
+            }
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            const int i = lane + 32 * s2;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+                if (i < M && c < n) Bs[c * (M + 1) + i] = b[s2][c];
+        }
+    }
+    __syncthreads();
+
+    for (int q = 0; q < nsys; ++q)
+        unstage_system<T, M>(g, base + q * per + M * M + M, sys0 + q, 0, n, tid, nthr);
+}
+
+// ---------------------------------------------------------------- alpha == 0
+// B <- 0 for every system, without reading A (BLAS convention).
+template <typename T>
+__global__ void zero_rhs_kernel(T *B, int64_t rows, int64_t cols, int64_t ld, int64_t stride, int64_t batch,
+                                int layout) {
+    const int64_t per = rows * cols;
+    const int64_t total = per * batch;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = e / per, r = e - b * per;
+        int64_t off;
+        if (layout == 0) off = (r / rows) * ld + (r % rows);  // column-major: r = j*rows + i
+        else off = (r / cols) * ld + (r % cols);              // row-major:    r = i*cols + j
+        B[b * stride + off] = zero_of<T>();
+    }
+}
+
+}  // namespace trsm

@@ -1,0 +1,6 @@
+// Small-regime (m <= 64) warp-per-system launches (n <= 8) for element type double2.
+#include "small_launch.cuh"
+
+namespace trsm {
+int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st) { return launch_rowlane_typed<double2>(a, st); }
+}  // namespace trsm
