@@ -93,6 +93,12 @@ def barrier(dist):
         dist.barrier()
 
 
+def weak_scaling_value(world_size, flops_per_rank_step, steps, max_rank_ms):
+    """Whole-job GFLOPS: every rank solves its own batches (no exchange), so
+    the work is world_size times one rank's, over the slowest rank's time."""
+    return world_size * flops_per_rank_step * steps / (max_rank_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
@@ -196,7 +202,9 @@ def run_gb300(args, ws, rank, local):
     torch.cuda.set_device(local)
     dist = init_dist(ws, "nccl")
     dev = torch.device("cuda", local)
-    tgb.build()
+    if rank == 0:
+        tgb.build()
+    barrier(dist)
     tg.load_library()
     m, n, batch = SQUARE["m"], SQUARE["n"], SQUARE["batch"]
     stream = torch.cuda.current_stream()
@@ -249,7 +257,7 @@ def run_gb300(args, ws, rank, local):
     kernel_ms_total = sum(sum(v) for v in per_dtype_ms.values())
     kernel_ms_max = reduce_max(dist, kernel_ms_total, dev)
     step_flops = sum(ti.flops(d, m, n, batch) for d in DTYPES)
-    value = ws * step_flops * args.steps / (kernel_ms_max * 1e-3) / 1e9
+    value = weak_scaling_value(ws, step_flops, args.steps, kernel_ms_max)
 
     # end to end through the public API: host buffers in pinned memory,
     # copies inside the timed region
@@ -517,6 +525,7 @@ def run_reference(args, ws, rank):
         "value": round(value, 3), "unit": "GFLOPS", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 accumulation (f32+f64+c64+c128 storage)", "data": "synthetic",
+        "n_gpus_requested": ws,
         "config": {"workload": "square64: m=n=64 column-major, batch sample per type", "sample": sample_txt},
         "cpu_baseline": {"value": round(value, 3), "unit": "GFLOPS", "cores": cores, "kind": "oracle",
                          "sample": sample_txt},

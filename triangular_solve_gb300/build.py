@@ -41,10 +41,12 @@ def _deps() -> list[str]:
 
 
 def _compile(src: str, obj: str, extra: list[str]) -> tuple[str, str]:
-    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    tmp = obj + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+    os.replace(tmp, obj)  # atomic: concurrent builders never see a partial object
     return src, r.stderr
 
 

@@ -38,17 +38,40 @@ struct SmallGeom {
     int w;    // RHS columns per CTA slice (colreg) / register columns (rowlane)
 };
 
+// Vector width (elements per 16-byte shared load).
+template <typename T> struct Vec { static constexpr int kN = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T); };
+
+// Packed lower triangle in shared memory.  Column k keeps rows
+// [s(k), M) with s(k) = k rounded down to the vector width V, so every
+// column starts 16-byte aligned and the strictly lower rows k+1.. are read
+// with 16-byte broadcast loads.  Rows s(k)..k of column k are never read.
+// Column k starts at off(k) = sum_{q<k} (M - s(q)); total (M^2 + M V)/2.
+template <typename T, int M>
+struct Packed {
+    static constexpr int V = Vec<T>::kN;
+    static __host__ __device__ constexpr int s(int k) { return (k / V) * V; }
+    static __host__ __device__ constexpr int off(int k) {
+        // sum_{q<k} s(q) = V * (V a (a-1)/2 + a b),  k = a V + b
+        return k * M - V * (V * (k / V) * (k / V - 1) / 2 + (k / V) * (k % V));
+    }
+    static constexpr int kSize = (M * M + M * V) / 2;
+    static_assert(off(M) == kSize, "packed size");
+    // pointer p such that p[i] is row i of column k (valid for i >= s(k))
+    static __device__ __forceinline__ const T *col(const T *Ls, int k) { return Ls + off(k) - s(k); }
+};
+
 // Shared-memory image of one system:
-//   Ls   M x M, column-major (ld M): the strictly lower part of L; the
-//        diagonal and everything above it hold zero.
+//   Ls   packed strictly-lower columns of L (see Packed); rows at or above
+//        the diagonal and padding rows >= m hold zero.
 //   dinv M reciprocals of the diagonal (zero for padding rows >= m).
 //   Bs   w columns of the RHS, column stride M + 1 (odd, so a thread per
 //        column reads its own column without bank conflicts).
 template <typename T, int M>
 struct SmallImage {
+    static constexpr int kLs = Packed<T, M>::kSize;
     static constexpr int kBld = M + 1;
     static __host__ __device__ __forceinline__ int elems(int w) {
-        const int e = M * M + M + w * kBld;
+        const int e = kLs + M + w * kBld;
         constexpr int a = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T);
         return (e + a - 1) / a * a;  // keep every system's Ls 16-byte aligned
     }
@@ -64,11 +87,14 @@ __device__ __forceinline__ void stage_system(const SmallGeom &g, T *Ls, T *dinv,
     const T *B = static_cast<const T *>(g.B) + sys * g.sB;
     const int m = g.m;
     const T z = zero_of<T>();
+    using P = Packed<T, M>;
     if (g.layout == 0) {
         for (int e = tid; e < M * M; e += nthr) {
             const int k = e / M, i = e - k * M;
-            if (i > k && i < m) cp_async<sizeof(T)>(Ls + e, A + (int64_t)k * g.lda + i);
-            else Ls[e] = z;
+            if (i < P::s(k)) continue;
+            T *d = Ls + P::off(k) + (i - P::s(k));
+            if (i > k && i < m) cp_async<sizeof(T)>(d, A + (int64_t)k * g.lda + i);
+            else *d = z;
         }
         for (int e = tid; e < wcols * M; e += nthr) {
             const int c = e / M, i = e - c * M;
@@ -79,8 +105,10 @@ __device__ __forceinline__ void stage_system(const SmallGeom &g, T *Ls, T *dinv,
     } else {
         for (int e = tid; e < M * M; e += nthr) {
             const int i = e / M, k = e - i * M;
-            if (i > k && i < m) cp_async<sizeof(T)>(Ls + k * M + i, A + (int64_t)i * g.lda + k);
-            else Ls[k * M + i] = z;
+            if (i < P::s(k)) continue;
+            T *d = Ls + P::off(k) + (i - P::s(k));
+            if (i > k && i < m) cp_async<sizeof(T)>(d, A + (int64_t)i * g.lda + k);
+            else *d = z;
         }
         for (int e = tid; e < wcols * M; e += nthr) {
             const int i = e / wcols, c = e - i * wcols;
@@ -109,9 +137,6 @@ __device__ __forceinline__ void unstage_system(const SmallGeom &g, const T *Bs, 
         }
     }
 }
-
-// Vector width (elements per 16-byte shared load).
-template <typename T> struct Vec { static constexpr int kN = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T); };
 
 template <typename T>
 __device__ __forceinline__ void lds16(const T *p, T (&out)[Vec<T>::kN]) {
@@ -155,7 +180,7 @@ struct DiagSteps {
             constexpr int k = CH * RC + KK;
             const T xk = mul(b[KK], dinv[k]);
             b[KK] = xk;
-            update_rows<T, RC, KK + 1>(Ls + k * M + CH * RC, xk, b);
+            update_rows<T, RC, KK + 1>(Packed<T, M>::col(Ls, k) + CH * RC, xk, b);
             DiagSteps<T, M, RC, CH, KK + 1>::run(Ls, dinv, b);
         }
     }
@@ -174,7 +199,7 @@ struct ColumnChunks {
 #pragma unroll
             for (int k = 0; k < CH * RC; ++k) {
                 const T xk = bs[k];
-                update_rows<T, RC, 0>(Ls + k * M + CH * RC, xk, b);
+                update_rows<T, RC, 0>(Packed<T, M>::col(Ls, k) + CH * RC, xk, b);
             }
             DiagSteps<T, M, RC, CH, 0>::run(Ls, dinv, b);
 #pragma unroll
@@ -186,6 +211,7 @@ struct ColumnChunks {
 
 template <typename T, int M, int RC>
 __global__ void __launch_bounds__(256) small_colreg_kernel(const SmallGeom g, const T alpha) {
+    static_assert(M % RC == 0, "row chunks must tile the column");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T *base = reinterpret_cast<T *>(smem_raw);
     const int w = g.w;
@@ -198,7 +224,8 @@ __global__ void __launch_bounds__(256) small_colreg_kernel(const SmallGeom g, co
 
     for (int s = 0; s < nsys; ++s) {
         T *Ls = base + s * per;
-        stage_system<T, M>(g, Ls, Ls + M * M, Ls + M * M + M, sys0 + s, j0, wcols, tid, nthr);
+        stage_system<T, M>(g, Ls, Ls + SmallImage<T, M>::kLs, Ls + SmallImage<T, M>::kLs + M, sys0 + s, j0,
+                           wcols, tid, nthr);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -206,13 +233,13 @@ __global__ void __launch_bounds__(256) small_colreg_kernel(const SmallGeom g, co
     const int s = tid / w, c = tid - s * w;
     if (s < nsys && c < wcols) {
         const T *Ls = base + s * per;
-        T *bs = base + s * per + M * M + M + c * (M + 1);
-        ColumnChunks<T, M, RC, 0>::run(Ls, Ls + M * M, bs, alpha);
+        T *bs = base + s * per + SmallImage<T, M>::kLs + M + c * (M + 1);
+        ColumnChunks<T, M, RC, 0>::run(Ls, Ls + SmallImage<T, M>::kLs, bs, alpha);
     }
     __syncthreads();
 
     for (int q = 0; q < nsys; ++q)
-        unstage_system<T, M>(g, base + q * per + M * M + M, sys0 + q, j0, wcols, tid, nthr);
+        unstage_system<T, M>(g, base + q * per + SmallImage<T, M>::kLs + M, sys0 + q, j0, wcols, tid, nthr);
 }
 
 // ---------------------------------------------------------------- rowlane
@@ -239,15 +266,16 @@ __global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, c
 
     for (int s = 0; s < nsys; ++s) {
         T *Ls = base + s * per;
-        stage_system<T, M>(g, Ls, Ls + M * M, Ls + M * M + M, sys0 + s, 0, n, tid, nthr);
+        stage_system<T, M>(g, Ls, Ls + SmallImage<T, M>::kLs, Ls + SmallImage<T, M>::kLs + M, sys0 + s, 0, n,
+                           tid, nthr);
     }
     cp_async_wait_all();
     __syncthreads();
 
     if (warp < nsys) {  // warp-uniform
         const T *Ls = base + warp * per;
-        const T *dinv = Ls + M * M;
-        T *Bs = base + warp * per + M * M + M;
+        const T *dinv = Ls + SmallImage<T, M>::kLs;
+        T *Bs = base + warp * per + SmallImage<T, M>::kLs + M;
         T b[S][NC];
 #pragma unroll
         for (int s2 = 0; s2 < S; ++s2) {
@@ -271,7 +299,7 @@ __global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, c
             for (int s2 = slot; s2 < S; ++s2) {
                 const int i = lane + 32 * s2;
                 if (i > k && i < M) {
-                    const T l = Ls[k * M + i];
+                    const T l = Packed<T, M>::col(Ls, k)[i];
 #pragma unroll
                     for (int c = 0; c < NC; ++c) b[s2][c] = fms(l, x[c], b[s2][c]);
                 }
@@ -288,7 +316,7 @@ __global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, c
     __syncthreads();
 
     for (int q = 0; q < nsys; ++q)
-        unstage_system<T, M>(g, base + q * per + M * M + M, sys0 + q, 0, n, tid, nthr);
+        unstage_system<T, M>(g, base + q * per + SmallImage<T, M>::kLs + M, sys0 + q, 0, n, tid, nthr);
 }
 
 // ---------------------------------------------------------------- alpha == 0

@@ -7,11 +7,13 @@
 namespace trsm {
 
 // Registers per thread bound the row chunk: a thread keeps RC elements of its
-// column live.  Complex double keeps 32 (64 doubles); the rest keep all 64.
+// column live.  Complex double keeps at most 32 (64 doubles) in chunks that
+// divide M; the other types keep the whole column.
 template <typename T, int M>
 constexpr int small_rc() {
-    return (sizeof(T) >= 16 && M > 32) ? 32 : M;
+    return (sizeof(T) >= 16 && M > 32) ? (M % 32 == 0 ? 32 : M / 2) : M;
 }
+static_assert(64 % small_rc<double2, 64>() == 0 && 48 % small_rc<double2, 48>() == 0, "chunks divide M");
 
 template <typename Kern>
 static int set_smem(Kern k, size_t bytes) {
@@ -40,7 +42,7 @@ static int launch_colreg_m(SmallGeom g, T alpha, cudaStream_t st) {
     const int w = g.n < 64 ? g.n : 64;
     const size_t per = (size_t)SmallImage<T, M>::elems(w) * sizeof(T);
     int spc = 128 / w > 1 ? 128 / w : 1;
-    while (spc > 1 && (size_t)spc * per > 110 * 1024) --spc;
+    while (spc > 1 && (size_t)spc * per > 225 * 1024) --spc;
     g.spc = spc;
     g.w = w;
     const size_t smem = (size_t)spc * per;
