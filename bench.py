@@ -534,6 +534,7 @@ def run_reference(args, ws, rank):
 
 
 def main():
+    global DTYPES
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -545,11 +546,14 @@ def main():
     ap.add_argument("--sweep-ms", default="1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-reps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtypes", default="f32,f64,c64,c128",
+                    help="subset of the step's types (profiling a single kernel)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     ws, rank, local = dist_env()
+    DTYPES = tuple(d for d in DTYPES if d in args.dtypes.split(","))
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return

@@ -181,14 +181,6 @@ int solve(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const 
 
 namespace trsm {
 
-size_t blocked_workspace_bytes(int elem, int64_t m, int64_t n, int64_t nb) {
-    int64_t wb, xb;
-    const int64_t tb = (m + nb - 1) / nb;
-    wb = ((tb * nb * nb * elem + 255) / 256) * 256;
-    xb = ((nb * (n > 0 ? n : 1) * elem + 255) / 256) * 256;
-    return (size_t)(wb + xb);
-}
-
 template <typename T>
 static int transpose_typed(const void *src, int64_t ld_src, void *dst, int64_t ld_dst, int64_t rows,
                            int64_t cols, cudaStream_t st) {

@@ -215,6 +215,8 @@ struct GemmArgs {
     int64_t ldc;
     T gamma, beta;
     int beta_zero, a_lower;
+    int b_rowmajor;  // B element (k, c) at k*ldb + c instead of c*ldb + k
+    int c_rowmajor;  // C element (r, c) at r*ldc + c instead of c*ldc + r
 };
 
 template <typename T>
@@ -242,11 +244,20 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
             if (gr < g.M && gk < kend) cp_async<sizeof(T)>(&As[s][kk][r], g.A + gk * g.lda + gr);
             else As[s][kk][r] = zero_of<T>();
         }
-        for (int e = tid; e < BK * BN; e += NT) {
-            const int kk = e % BK, c = e / BK;
-            const int64_t gc = n0 + c, gk = k0 + kk;
-            if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gc * g.ldb + gk);
-            else Bs[s][kk][c] = zero_of<T>();
+        if (g.b_rowmajor) {
+            for (int e = tid; e < BK * BN; e += NT) {
+                const int kk = e / BN, c = e % BN;
+                const int64_t gc = n0 + c, gk = k0 + kk;
+                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gk * g.ldb + gc);
+                else Bs[s][kk][c] = zero_of<T>();
+            }
+        } else {
+            for (int e = tid; e < BK * BN; e += NT) {
+                const int kk = e % BK, c = e / BK;
+                const int64_t gc = n0 + c, gk = k0 + kk;
+                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gc * g.ldb + gk);
+                else Bs[s][kk][c] = zero_of<T>();
+            }
         }
     };
 
@@ -288,23 +299,11 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
         for (int x = 0; x < TM; ++x) {
             const int64_t gr = m0 + tx * TM + x;
             if (gr >= g.M) continue;
-            T *cp = g.C + gc * g.ldc + gr;
+            T *cp = g.c_rowmajor ? g.C + gr * g.ldc + gc : g.C + gc * g.ldc + gr;
             T v = mul(g.gamma, acc[x][y]);
             if (!g.beta_zero) v = fma_(g.beta, *cp, v);
             *cp = v;
         }
-    }
-}
-
-// dst[r, c] = src[r, c] for an rows x cols column-major block.
-template <typename T>
-__global__ void copy_block_kernel(const T *__restrict__ src, int64_t lds, T *__restrict__ dst, int64_t ldd,
-                                  int64_t rows, int64_t cols) {
-    const int64_t total = rows * cols;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t c = e / rows, r = e - c * rows;
-        dst[c * ldd + r] = src[c * lds + r];
     }
 }
 

@@ -1,20 +1,13 @@
 // Host driver of the blocked path for one element type.
 #pragma once
 
+#include <type_traits>
+
 #include "blocked_kernels.cuh"
+#include "gemm_sp.cuh"
 #include "internal.h"
 
 namespace trsm {
-
-inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
-
-// Workspace: W (T_blocks x NB x NB inverted diagonal blocks) then an NB x n
-// panel for X_t, each 256-byte aligned.
-inline void blocked_ws_layout(int elem, int64_t m, int64_t n, int64_t nb, int64_t *w_bytes, int64_t *x_bytes) {
-    const int64_t tb = (m + nb - 1) / nb;
-    *w_bytes = round_up(tb * nb * nb * elem, 256);
-    *x_bytes = round_up(nb * (n > 0 ? n : 1) * elem, 256);
-}
 
 template <typename T>
 static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
@@ -23,6 +16,45 @@ static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
     const dim3 grid((unsigned)((g.M + C::BM - 1) / C::BM), (unsigned)((g.N + C::BN - 1) / C::BN));
     gemm_kernel<T><<<grid, 256, 0, st>>>(g);
     return launch_status();
+}
+
+// Trailing update C = beta*C - A X (A column-major, X row-major panel).
+template <typename T>
+static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t lda, const T *X, int64_t ldx,
+                         T *C, int64_t ldc, T beta, T minus_one, cudaStream_t st) {
+    if (M <= 0 || N <= 0) return TRSM_SUCCESS;
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
+        using Tl = SpTile<T>;
+        const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
+                             ((lda * (int64_t)sizeof(T)) % 16 == 0) && (K % Tl::BK == 0);
+        if (aligned) {
+            SpArgs g;
+            g.M = M; g.N = N; g.K = K;
+            g.A = A; g.lda = lda;
+            g.X = X; g.ldx = ldx;
+            g.C = C; g.ldc = ldc;
+            memcpy(&g.beta, &beta, sizeof(T));
+            auto kern = sp_update_kernel<T>;
+            if (Tl::SMEM > 48 * 1024) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
+            const dim3 grid((unsigned)((M + Tl::BM - 1) / Tl::BM), (unsigned)((N + Tl::BN - 1) / Tl::BN));
+            kern<<<grid, 256, Tl::SMEM, st>>>(g);
+            return launch_status();
+        }
+    }
+    GemmArgs<T> up;
+    up.M = M; up.N = N; up.K = K;
+    up.A = A; up.lda = lda;
+    up.B = X; up.ldb = ldx;
+    up.C = C; up.ldc = ldc;
+    up.gamma = minus_one;
+    up.beta = beta;
+    up.beta_zero = 0; up.a_lower = 0;
+    up.b_rowmajor = 1; up.c_rowmajor = 0;
+    return gemm_launch<T>(up, st);
 }
 
 template <typename T, int IB>
@@ -83,10 +115,10 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     T *B = static_cast<T *>(a.B);
     T alpha;
     memcpy(&alpha, a.alpha, sizeof(T));
-    int64_t wb, xb;
-    blocked_ws_layout((int)sizeof(T), m, n, nb, &wb, &xb);
+    const int64_t tbk = (m + nb - 1) / nb;
+    const int64_t ldx = panel_ld(n);
     T *W = static_cast<T *>(a.ws);
-    T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + wb);
+    T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + round256(tbk * nb * nb * (int64_t)sizeof(T)));
 
     PhaseTimer timer;
     int rc = TRSM_SUCCESS;
@@ -118,9 +150,10 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         ap.M = mb; ap.N = n; ap.K = mb;
         ap.A = W + t * nb * nb; ap.lda = nb;
         ap.B = B + r0; ap.ldb = a.ldb;
-        ap.C = Xw; ap.ldc = nb;
+        ap.C = Xw; ap.ldc = ldx;
         ap.gamma = (t == 0) ? alpha : one;
         ap.beta = one; ap.beta_zero = 1; ap.a_lower = 1;
+        ap.b_rowmajor = 0; ap.c_rowmajor = 1;
         timer.begin();
         if ((rc = gemm_launch<T>(ap, st))) return rc;
         if ((rc = timer.end(1))) return rc;
@@ -130,21 +163,16 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         // and X_t back into its block row of B.
         timer.begin();
         if (r0 + nb < m) {
-            GemmArgs<T> up;
-            up.M = m - r0 - nb; up.N = n; up.K = nb;
-            up.A = L + r0 * a.lda + r0 + nb; up.lda = a.lda;
-            up.B = Xw; up.ldb = nb;
-            up.C = B + r0 + nb; up.ldc = a.ldb;
-            up.gamma = minus_one;
-            up.beta = (t == 0) ? alpha : one;
-            up.beta_zero = 0; up.a_lower = 0;
-            if ((rc = gemm_launch<T>(up, st))) return rc;
+            const T beta = (t == 0) ? alpha : one;
+            const T *Lp = L + r0 * a.lda + r0 + nb;
+            if ((rc = update_launch<T>(m - r0 - nb, n, nb, Lp, a.lda, Xw, ldx, B + r0 + nb, a.ldb, beta,
+                                       minus_one, st)))
+                return rc;
         }
         {
-            const int64_t total = mb * n;
-            int64_t blocks = (total + 255) / 256;
-            if (blocks > 152 * 8) blocks = 152 * 8;
-            copy_block_kernel<T><<<(unsigned)blocks, 256, 0, st>>>(Xw, nb, B + r0, a.ldb, mb, n);
+            // X_t (row-major panel) back into its block row of B (column-major)
+            const dim3 grid((unsigned)((n + 31) / 32), (unsigned)((mb + 31) / 32));
+            transpose_kernel<T><<<grid, dim3(32, 8), 0, st>>>(Xw, ldx, B + r0, a.ldb, mb, n);
             if ((rc = launch_status())) return rc;
         }
         if ((rc = timer.end(2))) return rc;

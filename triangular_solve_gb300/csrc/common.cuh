@@ -71,6 +71,12 @@ __device__ __forceinline__ double2 fma_(double2 a, double2 b, double2 c) {
     return make_double2(re, im);
 }
 
+// a - b
+__device__ __forceinline__ float sub_(float a, float b) { return a - b; }
+__device__ __forceinline__ double sub_(double a, double b) { return a - b; }
+__device__ __forceinline__ float2 sub_(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ double2 sub_(double2 a, double2 b) { return make_double2(a.x - b.x, a.y - b.y); }
+
 // 1 / d.  Real: the IEEE division operator.  Complex: Smith's 1962 method
 // (R. L. Smith, "Algorithm 116: Complex division", CACM 5(8)), which scales
 // by the larger of |re|, |im| so that the squared modulus is never formed.

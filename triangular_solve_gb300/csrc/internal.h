@@ -49,8 +49,15 @@ struct BlockedArgs {
     float *ms;       // optional: per-phase milliseconds (profiling entry)
 };
 
-// Bytes of workspace the blocked path needs.
-size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb);
+// Bytes of workspace the blocked path needs: the inverted diagonal blocks
+// (ceil(m/nb) x nb x nb) then the X_t panel (nb x panel_ld(n), row-major),
+// each rounded up to 256 bytes.
+inline int64_t panel_ld(int64_t n) { return ((n > 0 ? n : 1) + 3) / 4 * 4; }
+inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+inline size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb) {
+    const int64_t tb = (m + nb - 1) / nb;
+    return (size_t)(round256(tb * nb * nb * elem_bytes) + round256(nb * panel_ld(n) * elem_bytes));
+}
 
 int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);
 int blocked_solve_f64(const BlockedArgs &a, cudaStream_t st);
