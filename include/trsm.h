@@ -146,6 +146,39 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
                       const void *A, int64_t lda, void *B, int64_t ldb, int64_t nb,
                       void *workspace, size_t ws_bytes, void *stream, float *ms);
 
+/*
+ * Size in bytes of the device array trsm_llnn_noalloc uses as its workspace
+ * (32 MiB; every GPU that loads the library holds it until the process
+ * exits).
+ */
+#define TRSM_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
+
+/*
+ * trsm_llnn for callers that cannot allocate device memory -- for example a
+ * library embedded in a host application that owns all device memory
+ * through its own pool, or a latency-sensitive path on which cudaMalloc and
+ * cudaFree (which may synchronise the device) are not acceptable.  The
+ * pages describe no such entry point; it has no counterpart there.
+ *
+ * Same operation, arguments and validation as trsm_llnn (1 dtype, 2 m, 3 n,
+ * 4 alpha, 5 A, 6 lda, 7 B, 8 ldb, 9 stream; column-major, one system), but
+ * the call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  m <= 64 needs no workspace.  For m > 64 the blocked path's
+ * workspace lives in a fixed device array of TRSM_NOALLOC_SCRATCH_BYTES
+ * inside the library; a problem whose workspace
+ * (trsm_llnn_workspace_bytes(dtype, m, n, 0)) exceeds it is rejected with
+ * TRSM_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents (nothing in it needs to start
+ * at zero), so calls whose GPU work overlaps -- unordered streams, or
+ * several host threads -- race on it and must be serialised by the caller.
+ */
+int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
+                      const void *A, int64_t lda, void *B, int64_t ldb, void *stream);
+
 /* Static, human-readable text for a status code returned by this library. */
 const char *trsm_status_string(int status);
 

@@ -189,6 +189,24 @@ def trsm_llnn_profile(dtype, m, n, alpha, A, lda, B, ldb, nb, workspace, ws_byte
     return float(ms[0]), float(ms[1]), float(ms[2])
 
 
+def trsm_llnn_noalloc(dtype, m, n, alpha, A, lda, B, ldb, stream=None) -> None:
+    """trsm_llnn that allocates no device memory: the blocked path's workspace
+    is a fixed array inside the library (see include/trsm.h).  For callers
+    whose host application owns all device memory, or whose path must not
+    call cudaMalloc / cudaFree."""
+    lib = load_library()
+    fn = lib.trsm_llnn_noalloc
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    fn.argtypes = [ctypes.c_int, i64, i64, vp, vp, i64, vp, i64, vp]
+    fn.restype = ctypes.c_int
+    code = _dtype_code(dtype)
+    al, _ = _alpha_buf(code, alpha)
+    _check("trsm_llnn_noalloc", fn(code, m, n, al, _ptr(A), lda, _ptr(B), ldb, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
 def trsm_status_string(status: int) -> str:
     return load_library().trsm_status_string(int(status)).decode()
 
