@@ -357,10 +357,10 @@ def run_gb300(args, ws, rank, local):
 
 
 def run_large(torch, tg, dev, stream, peaks, reps=2):
-    """Blocked-path workloads: m = n = 16384 in f32 and complex64 (table NB)."""
+    """Blocked-path workloads with the table's NB: m = n = 16384 in f32 and
+    complex64 (alpha = 1), m = n = 8192 in f64 and complex128 (alpha = 1.5)."""
     res = {}
-    for d in ("f32", "c64"):
-        mm = 16384
+    for d, mm, alpha in (("f32", 16384, 1.0), ("c64", 16384, 1.0), ("f64", 8192, 1.5), ("c128", 8192, 1.5)):
         L, B = ti.generate(d, mm, mm, 1, kind="ddm")
         a = torch.from_numpy(ti.to_storage(L, "col")).to(dev)
         b0 = torch.from_numpy(ti.to_storage(B, "col")).to(dev)
@@ -370,24 +370,26 @@ def run_large(torch, tg, dev, stream, peaks, reps=2):
         wsb = tg.trsm_llnn_workspace_bytes(d, mm, mm, nb)
         wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
         b.copy_(b0)
-        tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)  # warm-up
+        tg.trsm_llnn_ex(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)  # warm-up
         times, phases = [], []
         for _ in range(reps):
             b.copy_(b0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            tg.trsm_llnn_ex(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+            tg.trsm_llnn_ex(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)
             e1.record(stream)
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
         b.copy_(b0)
-        phases = tg.trsm_llnn_profile(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+        phases = tg.trsm_llnn_profile(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)
         ms = statistics.mean(times)
         gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
         tot = sum(phases)
+        fp64 = d in ("f64", "c128")
         res[f"{d}_m{mm}"] = {
             "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1),
-            "frac_of_fp32_alu_peak": round(gf / 1e3 / fp32_alu_peak_tflops(), 4),
+            "pipe": "FP64 (DFMA)" if fp64 else "FP32 (FFMA)",
+            "frac_of_pipe_peak": round(gf / 1e3 / (FP64_PEAK_TFLOPS if fp64 else fp32_alu_peak_tflops()), 4),
             "phase_share": {"diag_inversion": round(phases[0] / tot, 4),
                             "block_apply": round(phases[1] / tot, 4),
                             "gemm_update": round(phases[2] / tot, 4)},

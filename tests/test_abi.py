@@ -46,13 +46,13 @@ def test_select_nb_table(lib):
 def test_workspace_bytes(lib):
     assert tg.trsm_llnn_workspace_bytes("f32", 64, 64) == 0
     assert tg.trsm_llnn_workspace_bytes("f32", 1000, 0) == 0
-    # m = 1000, NB = 128: 8 blocks of 128 x 128 plus a 128 x 72 panel (row
+    # m = 1000, NB = 128: 8 blocks of 128 x 128 plus two 128 x 72 panels (row
     # length rounded up to 4 elements), 4 bytes
     w = 8 * 128 * 128 * 4
     x = 128 * 72 * 4
     r = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    assert tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 128) == r(w) + r(x)
-    assert tg.trsm_llnn_workspace_bytes("c128", 1000, 70, 512) == r(2 * 512 * 512 * 16) + r(512 * 72 * 16)
+    assert tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 128) == r(w) + 2 * r(x)
+    assert tg.trsm_llnn_workspace_bytes("c128", 1000, 70, 512) == r(2 * 512 * 512 * 16) + 2 * r(512 * 72 * 16)
     with pytest.raises(ValueError):
         tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 100)
 

@@ -151,3 +151,12 @@ def test_solve_convenience_with_torch_layouts(env):
     tB2 = torch.from_numpy(B.copy()).cuda().transpose(1, 2).contiguous().transpose(1, 2)
     tg.solve(tA2, tB2)
     assert float(per_system_rel_fro(tB2.cpu().numpy(), ref).max()) <= TOL["c64"]
+
+
+@pytest.mark.parametrize("m,n,batch", [(64, 70, 700), (32, 100, 1000), (48, 64, 612), (16, 200, 700)])
+def test_persistent_f32_path_many_items(env, m, n, batch):
+    """Enough (system, 64-column slice) items for the persistent pipelined
+    f32 kernel, with a ragged last slice and items not divisible by the
+    warps in flight."""
+    L, B = ti.generate("f32", m, n, batch, kind="dd64", seed=m + n)
+    _parity(env, "f32", L, B, 0.5, f"pipe m={m} n={n} batch={batch}")

@@ -33,7 +33,12 @@ static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t ld
             g.A = A; g.lda = lda;
             g.X = X; g.ldx = ldx;
             g.C = C; g.ldc = ldc;
+            g.beta = make_float2(0.f, 0.f);
+            g.gamma = make_float2(0.f, 0.f);
             memcpy(&g.beta, &beta, sizeof(T));
+            memcpy(&g.gamma, &minus_one, sizeof(T));
+            g.beta_zero = 0;
+            g.k_by_col = 0;
             auto kern = sp_update_kernel<T>;
             if (Tl::SMEM > 48 * 1024) {
                 const cudaError_t e =
@@ -55,6 +60,47 @@ static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t ld
     up.beta_zero = 0; up.a_lower = 0;
     up.b_rowmajor = 1; up.c_rowmajor = 0;
     return gemm_launch<T>(up, st);
+}
+
+// Block apply for the single-precision types on the update kernel:
+//   X_t^T = gamma * R_t^T * (D_t^{-1})^T,
+// with R_t^T the row-major panel P (= a column-major n x mb matrix, ld ldx)
+// and (D_t^{-1})^T read as a row-major mb x mb matrix from W_t (column-
+// major, ld nb); the result, column-major n x mb with ld ldx, is the
+// row-major X_t panel.  (D_t^{-1})^T is upper triangular, so a column tile
+// stops its K loop at the tile's last column.  Returns kSpNotApplicable when
+// the operands are not 16-byte aligned.
+constexpr int kSpNotApplicable = -200000;
+template <typename T>
+static int apply_sp_launch(int64_t mb, int64_t n, const T *Wt, int64_t nb, const T *P, int64_t ldx, T *Xw, T gamma,
+                           cudaStream_t st) {
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
+        using Tl = SpTile<T>;
+        if (((reinterpret_cast<uintptr_t>(Wt) | reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(Xw)) &
+             15) != 0 || (nb * (int64_t)sizeof(T)) % 16 || (ldx * (int64_t)sizeof(T)) % 16)
+            return kSpNotApplicable;
+        SpArgs g;
+        g.M = n; g.N = mb; g.K = mb;
+        g.A = P; g.lda = ldx;
+        g.X = Wt; g.ldx = nb;
+        g.C = Xw; g.ldc = ldx;
+        g.beta = make_float2(0.f, 0.f);
+        g.gamma = make_float2(0.f, 0.f);
+        memcpy(&g.gamma, &gamma, sizeof(T));
+        g.beta_zero = 1;
+        g.k_by_col = 1;
+        auto kern = sp_update_kernel<T>;
+        if (Tl::SMEM > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        const dim3 grid((unsigned)((n + Tl::BM - 1) / Tl::BM), (unsigned)((mb + Tl::BN - 1) / Tl::BN));
+        kern<<<grid, 256, Tl::SMEM, st>>>(g);
+        return launch_status();
+    } else {
+        (void)mb; (void)n; (void)Wt; (void)nb; (void)P; (void)ldx; (void)Xw; (void)gamma; (void)st;
+        return kSpNotApplicable;
+    }
 }
 
 template <typename T, int IB>
@@ -119,6 +165,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     const int64_t ldx = panel_ld(n);
     T *W = static_cast<T *>(a.ws);
     T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + round256(tbk * nb * nb * (int64_t)sizeof(T)));
+    T *Pw = reinterpret_cast<T *>(reinterpret_cast<char *>(Xw) + round256(nb * ldx * (int64_t)sizeof(T)));
 
     PhaseTimer timer;
     int rc = TRSM_SUCCESS;
@@ -146,16 +193,28 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         const int64_t mb = (m - r0 < nb) ? m - r0 : nb;
         // Phase 1: X_t = gamma * D_t^{-1} R_t into the panel (gamma = alpha at
         // t = 0; later block rows already carry alpha through the updates).
-        GemmArgs<T> ap;
-        ap.M = mb; ap.N = n; ap.K = mb;
-        ap.A = W + t * nb * nb; ap.lda = nb;
-        ap.B = B + r0; ap.ldb = a.ldb;
-        ap.C = Xw; ap.ldc = ldx;
-        ap.gamma = (t == 0) ? alpha : one;
-        ap.beta = one; ap.beta_zero = 1; ap.a_lower = 1;
-        ap.b_rowmajor = 0; ap.c_rowmajor = 1;
+        const T gamma = (t == 0) ? alpha : one;
         timer.begin();
-        if ((rc = gemm_launch<T>(ap, st))) return rc;
+        rc = kSpNotApplicable;
+        if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
+            // R_t (column-major block row of B) -> row-major panel P
+            const dim3 tgrid((unsigned)((mb + 31) / 32), (unsigned)((n + 31) / 32));
+            transpose_kernel<T><<<tgrid, dim3(32, 8), 0, st>>>(B + r0, a.ldb, Pw, ldx, n, mb);
+            if ((rc = launch_status())) return rc;
+            rc = apply_sp_launch<T>(mb, n, W + t * nb * nb, nb, Pw, ldx, Xw, gamma, st);
+        }
+        if (rc == kSpNotApplicable) {
+            GemmArgs<T> ap;
+            ap.M = mb; ap.N = n; ap.K = mb;
+            ap.A = W + t * nb * nb; ap.lda = nb;
+            ap.B = B + r0; ap.ldb = a.ldb;
+            ap.C = Xw; ap.ldc = ldx;
+            ap.gamma = gamma;
+            ap.beta = one; ap.beta_zero = 1; ap.a_lower = 1;
+            ap.b_rowmajor = 0; ap.c_rowmajor = 1;
+            rc = gemm_launch<T>(ap, st);
+        }
+        if (rc) return rc;
         if ((rc = timer.end(1))) return rc;
 
         // Phase 2: trailing update  B[r0+nb:, :] = beta*B[...] - L[r0+nb:, r0:r0+nb] X_t

@@ -104,6 +104,27 @@ __device__ __forceinline__ double2 recip(double2 d) { return recip_smith<double2
 template <typename T> __device__ __forceinline__ T ldg(const T *p) { return __ldg(p); }
 
 // ----------------------------------------------------------------------------
+// Paired FP32 arithmetic (fma.rn.f32x2, sm_100 and later): two independent
+// single-precision FMAs in one instruction, operands packed in 64 bits
+// (low half = first element).  Halves the issue slots of FP32 FMA work.
+// ----------------------------------------------------------------------------
+using f32x2 = unsigned long long;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// a * b + c, element-wise on both halves
+__device__ __forceinline__ f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// ----------------------------------------------------------------------------
 // cp.async (LDGSTS): global -> shared copies that bypass registers.  Sizes
 // 4, 8 and 16 bytes; both addresses must be aligned to the size.
 // ----------------------------------------------------------------------------

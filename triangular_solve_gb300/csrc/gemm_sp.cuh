@@ -1,5 +1,5 @@
 // Trailing-update GEMM for the single-precision types (f32, complex64):
-//     C = beta * C - A * X
+//     C = beta * C + gamma * A * X      (update: gamma = -1)
 // A: M x K column-major (the L panel under the diagonal block), X: K x N
 // row-major (the X_t panel), C: M x N column-major (the block rows of B
 // below the panel).  This contraction is the dominant cost of the blocked
@@ -48,7 +48,9 @@ struct SpArgs {
     int64_t ldx;
     void *C;
     int64_t ldc;
-    float2 beta;  // beta.x used for real
+    float2 beta, gamma;  // C = beta*C + gamma*A*X (.x only for real)
+    int beta_zero;       // do not read C
+    int k_by_col;        // X(k, c) = 0 for k > c: column tile [n0, n0+BN) stops K at n0 + BN
 };
 
 // 16-byte copy of src_bytes (0..16) with zero fill of the rest.
@@ -60,6 +62,59 @@ __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, i
 
 __device__ __forceinline__ float beta_of(float2 b, float) { return b.x; }
 __device__ __forceinline__ float2 beta_of(float2 b, float2) { return b; }
+
+// Register tile of a thread.  f32 keeps row pairs packed for fma.rn.f32x2:
+// rows 2p and 2p+1 of a column share one 64-bit register pair, the A pair
+// comes straight from the 16-byte shared load and the X value is duplicated
+// once per k; complex64 keeps plain complex accumulators.
+template <typename E, int RM, int RN> struct AccTile;
+template <int RM, int RN>
+struct AccTile<float, RM, RN> {
+    f32x2 v[RM / 2][RN];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < RM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < RN; ++j) v[i][j] = 0ull;
+    }
+    // a: RM values in 16-byte chunks (as loaded), x: RN values
+    __device__ __forceinline__ void fma(const float4 (&a)[RM / 4], const float (&x)[RN]) {
+#pragma unroll
+        for (int j = 0; j < RN; ++j) {
+            const f32x2 xd = pack2(x[j], x[j]);
+#pragma unroll
+            for (int q = 0; q < RM / 4; ++q) {
+                const ulonglong2 ap = *reinterpret_cast<const ulonglong2 *>(&a[q]);
+                v[2 * q][j] = ffma2(ap.x, xd, v[2 * q][j]);
+                v[2 * q + 1][j] = ffma2(ap.y, xd, v[2 * q + 1][j]);
+            }
+        }
+    }
+    __device__ __forceinline__ float get(int i, int j) const {
+        float lo, hi;
+        unpack2(v[i / 2][j], lo, hi);
+        return (i & 1) ? hi : lo;
+    }
+};
+template <int RM, int RN>
+struct AccTile<float2, RM, RN> {
+    float2 v[RM][RN];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+            for (int j = 0; j < RN; ++j) v[i][j] = make_float2(0.f, 0.f);
+    }
+    __device__ __forceinline__ void fma(const float4 (&a)[RM / 2], const float2 (&x)[RN]) {
+#pragma unroll
+        for (int i = 0; i < RM; ++i) {
+            const float2 ai = reinterpret_cast<const float2 *>(&a[i / 2])[i & 1];
+#pragma unroll
+            for (int j = 0; j < RN; ++j) v[i][j] = fma_(ai, x[j], v[i][j]);
+        }
+    }
+    __device__ __forceinline__ float2 get(int i, int j) const { return v[i][j]; }
+};
 
 template <typename E>
 __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
@@ -77,7 +132,9 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
     const int wm = warp & 1, wn = warp >> 1;
     const int lx = lane & 7, ly = lane >> 3;
     const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN;
-    const int nk = (int)(g.K / BK);  // K is a multiple of BK (the block size NB)
+    int64_t kend = g.K;
+    if (g.k_by_col && n0 + BN < kend) kend = n0 + BN;
+    const int nk = (int)((kend + BK - 1) / BK);
 
     // one stage: A chunk rows are contiguous (column-major), X chunk columns
     // are contiguous (row-major)
@@ -91,7 +148,7 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
             const int kk = c / (BM / VE), r = (c % (BM / VE)) * VE;
             const int64_t gr = m0 + r;
             int bytes = 0;
-            if (gr < g.M) bytes = (int)((g.M - gr < VE ? g.M - gr : VE) * sizeof(E));
+            if (gr < g.M && k0 + kk < kend) bytes = (int)((g.M - gr < VE ? g.M - gr : VE) * sizeof(E));
             const E *src = bytes ? A + (k0 + kk) * g.lda + gr : A;
             cp_async16_zfill(as + kk * BM + r, src, bytes);
         }
@@ -100,17 +157,14 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
             const int kk = c / (BN / VE), col = (c % (BN / VE)) * VE;
             const int64_t gc = n0 + col;
             int bytes = 0;
-            if (gc < g.N) bytes = (int)((g.N - gc < VE ? g.N - gc : VE) * sizeof(E));
+            if (gc < g.N && k0 + kk < kend) bytes = (int)((g.N - gc < VE ? g.N - gc : VE) * sizeof(E));
             const E *src = bytes ? X + (k0 + kk) * g.ldx + gc : X;
             cp_async16_zfill(xs + kk * BN + col, src, bytes);
         }
     };
 
-    E acc[RM][RN];
-#pragma unroll
-    for (int i = 0; i < RM; ++i)
-#pragma unroll
-        for (int j = 0; j < RN; ++j) acc[i][j] = zero_of<E>();
+    AccTile<E, RM, RN> acc;
+    acc.zero();
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
@@ -134,14 +188,11 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
         const E *xs = Xs + (kt % STAGES) * Tl::X_STAGE;
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            E a[RM], x[RN];
+            float4 a[RM / VE];
+            E x[RN];
 #pragma unroll
-            for (int q = 0; q < RM / VE; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(as + kk * BM + a_off + q * 8 * VE);
-                const E *e = reinterpret_cast<const E *>(&v);
-#pragma unroll
-                for (int u = 0; u < VE; ++u) a[q * VE + u] = e[u];
-            }
+            for (int q = 0; q < RM / VE; ++q)
+                a[q] = *reinterpret_cast<const float4 *>(as + kk * BM + a_off + q * 8 * VE);
 #pragma unroll
             for (int q = 0; q < RN / VE; ++q) {
                 const float4 v = *reinterpret_cast<const float4 *>(xs + kk * BN + x_off + q * 4 * VE);
@@ -149,17 +200,16 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
 #pragma unroll
                 for (int u = 0; u < VE; ++u) x[q * VE + u] = e[u];
             }
-#pragma unroll
-            for (int i = 0; i < RM; ++i)
-#pragma unroll
-                for (int j = 0; j < RN; ++j) acc[i][j] = fma_(a[i], x[j], acc[i][j]);
+            acc.fma(a, x);
         }
     }
     cp_async_wait_all();
 
-    // epilogue: C = beta*C - acc, column by column (a thread's rows come in
-    // chunks of VE consecutive rows: one 16-byte access where aligned)
+    // epilogue: C = beta*C + gamma*acc, column by column (a thread's rows
+    // come in chunks of VE consecutive rows: one 16-byte access where aligned)
     const E beta = beta_of(g.beta, E{});
+    const E gamma = beta_of(g.gamma, E{});
+    const bool bz = g.beta_zero != 0;
     const bool vec_ok = ((g.ldc * (int64_t)sizeof(E)) % 16 == 0) &&
                         ((reinterpret_cast<uintptr_t>(Cm) & 15) == 0);
 #pragma unroll
@@ -171,15 +221,21 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
         for (int q = 0; q < RM / VE; ++q) {
             const int64_t gr0 = m0 + wm * Tl::WM + q * 8 * VE + lx * VE;
             if (vec_ok && gr0 + VE <= g.M) {
-                float4 v = *reinterpret_cast<const float4 *>(ccol + gr0);
+                float4 v = bz ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4 *>(ccol + gr0);
                 E *e = reinterpret_cast<E *>(&v);
 #pragma unroll
-                for (int u = 0; u < VE; ++u) e[u] = sub_(mul(beta, e[u]), acc[q * VE + u][j]);
+                for (int u = 0; u < VE; ++u) {
+                    const E t = mul(gamma, acc.get(q * VE + u, j));
+                    e[u] = bz ? t : fma_(beta, e[u], t);
+                }
                 *reinterpret_cast<float4 *>(ccol + gr0) = v;
             } else {
 #pragma unroll
                 for (int u = 0; u < VE; ++u)
-                    if (gr0 + u < g.M) ccol[gr0 + u] = sub_(mul(beta, ccol[gr0 + u]), acc[q * VE + u][j]);
+                    if (gr0 + u < g.M) {
+                        const E t = mul(gamma, acc.get(q * VE + u, j));
+                        ccol[gr0 + u] = bz ? t : fma_(beta, ccol[gr0 + u], t);
+                    }
             }
         }
     }

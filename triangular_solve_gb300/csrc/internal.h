@@ -31,6 +31,14 @@ int launch_rowlane_f64(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_c64(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st);
 
+// Fast path of the thread-per-column kernel for aligned full-size systems
+// (m in {8, 16, 32, 48, 64}); returns kFastNotApplicable (-100000) when its
+// preconditions do not hold.
+int launch_fast_f32(const SmallArgs &a, cudaStream_t st);
+int launch_fast_f64(const SmallArgs &a, cudaStream_t st);
+int launch_fast_c64(const SmallArgs &a, cudaStream_t st);
+int launch_fast_c128(const SmallArgs &a, cudaStream_t st);
+
 // alpha == 0: B <- 0 without reading A.
 int launch_zero_f32(const SmallArgs &a, cudaStream_t st);
 int launch_zero_f64(const SmallArgs &a, cudaStream_t st);
@@ -50,13 +58,14 @@ struct BlockedArgs {
 };
 
 // Bytes of workspace the blocked path needs: the inverted diagonal blocks
-// (ceil(m/nb) x nb x nb) then the X_t panel (nb x panel_ld(n), row-major),
-// each rounded up to 256 bytes.
+// (ceil(m/nb) x nb x nb), then two nb x panel_ld(n) row-major panels (X_t,
+// and the transposed block row R_t the single-precision apply reads), each
+// rounded up to 256 bytes.
 inline int64_t panel_ld(int64_t n) { return ((n > 0 ? n : 1) + 3) / 4 * 4; }
 inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 inline size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb) {
     const int64_t tb = (m + nb - 1) / nb;
-    return (size_t)(round256(tb * nb * nb * elem_bytes) + round256(nb * panel_ld(n) * elem_bytes));
+    return (size_t)(round256(tb * nb * nb * elem_bytes) + 2 * round256(nb * panel_ld(n) * elem_bytes));
 }
 
 int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);

@@ -3,6 +3,9 @@
 #include "small_launch.cuh"
 
 namespace trsm {
-int launch_colreg_c64(const SmallArgs &a, cudaStream_t st) { return launch_colreg_typed<float2>(a, st); }
+int launch_colreg_c64(const SmallArgs &a, cudaStream_t st) {
+    const int rc = launch_fast_c64(a, st);
+    return rc == -100000 ? launch_colreg_typed<float2>(a, st) : rc;
+}
 int launch_zero_c64(const SmallArgs &a, cudaStream_t st) { return launch_zero_typed<float2>(a, st); }
 }  // namespace trsm

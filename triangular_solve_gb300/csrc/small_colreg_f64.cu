@@ -3,6 +3,9 @@
 #include "small_launch.cuh"
 
 namespace trsm {
-int launch_colreg_f64(const SmallArgs &a, cudaStream_t st) { return launch_colreg_typed<double>(a, st); }
+int launch_colreg_f64(const SmallArgs &a, cudaStream_t st) {
+    const int rc = launch_fast_f64(a, st);
+    return rc == -100000 ? launch_colreg_typed<double>(a, st) : rc;
+}
 int launch_zero_f64(const SmallArgs &a, cudaStream_t st) { return launch_zero_typed<double>(a, st); }
 }  // namespace trsm
