@@ -99,7 +99,10 @@ def test_noalloc_small_regime_needs_no_workspace(env):
 
 def test_noalloc_rejects_problems_beyond_its_array(env):
     torch = env["torch"]
-    m = n = 4096  # complex128: 64 MiB of workspace, twice the array
+    # complex128, m = n = 16384: the two X panels alone (2 x NB x n x 16 bytes)
+    # exceed the 32 MiB array for every block size, so the call must be
+    # rejected before anything is launched (the buffers below are tiny)
+    m = n = 16384
     need = env["lib"].trsm_llnn_workspace_bytes(CODE["c128"], m, n, 0)
     assert need > SCRATCH_BYTES
     a = torch.zeros(1, dtype=torch.complex128, device="cuda")
