@@ -445,7 +445,11 @@ def nb_sweep(args):
                     ts.append(e0.elapsed_time(e1))
                 ms = statistics.mean(ts)
                 gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
-                rows.append({"dtype": d, "m": mm, "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1)})
+                b.copy_(b0)
+                ph = tg.trsm_llnn_profile(d, mm, mm, 1.0, a, mm, b, mm, nb, wsp, wsb, stream)
+                tot = sum(ph) or 1.0
+                rows.append({"dtype": d, "m": mm, "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1),
+                             "phase_share": [round(v / tot, 4) for v in ph]})
                 print(json.dumps(rows[-1]), flush=True)
                 if best is None or gf > best[1]:
                     best = (nb, gf)

@@ -87,13 +87,15 @@ __global__ void __launch_bounds__(IB) inv_diag_l1_kernel(const T *__restrict__ L
 }
 
 // ---------------------------------------------------------------------------
-// Level 2: off-diagonal sub-blocks of W_t = D_t^{-1} along the wavefront
-// d = i - j (launched for d = 1..7 in order).  With S_ii the diagonal
-// sub-blocks and L_ik the sub-blocks of D_t,
+// Level 2: off-diagonal sub-blocks of W_t = D_t^{-1}.  With S_ii the
+// diagonal sub-blocks and L_ik the sub-blocks of D_t,
 //     Y_ij = -Y_ii * sum_{k=j}^{i-1} L_ik Y_kj ,
-// every Y_kj on the right lying on an earlier wavefront.  CTA (t, j) forms
-// P = L[i-rows, j..i-1 cols] * Y[j..i-1 rows, j col] (K = d*IB) in shared
-// memory, then Y_ij = -Y_ii * P.  256 threads, each owning a TR x TC patch.
+// every Y_kj on the right lying in the same block column j, above row
+// block i.  CTA (t, j) therefore walks down its block column, i = j+1 .. 7,
+// in one launch: for each i it forms P = L[i-rows, j..i-1 cols] *
+// Y[j..i-1 rows, j col] (K = (i-j)*IB) in shared memory, then
+// Y_ij = -Y_ii * P, and a block barrier publishes Y_ij to the next i.
+// 256 threads, each owning a TR x TC patch.
 // ---------------------------------------------------------------------------
 template <typename T, int IB>
 struct L2Cfg {
@@ -105,8 +107,8 @@ struct L2Cfg {
 };
 
 template <typename T, int IB>
-__global__ void __launch_bounds__(256) inv_offdiag_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
-                                                          T *__restrict__ W, int d) {
+__device__ __forceinline__ void inv_offdiag_block(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
+                                                  T *__restrict__ W, int d) {
     using C = L2Cfg<T, IB>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T *La = reinterpret_cast<T *>(smem_raw);  // [KC][IB]  (k-major chunk of L rows)
@@ -188,6 +190,15 @@ __global__ void __launch_bounds__(256) inv_offdiag_kernel(const T *__restrict__ 
 }
 
 template <typename T, int IB>
+__global__ void __launch_bounds__(256) inv_offdiag_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
+                                                          T *__restrict__ W) {
+    for (int d = 1; d < 8 - (int)blockIdx.y; ++d) {
+        inv_offdiag_block<T, IB>(L, lda, m, nb, W, d);
+        __syncthreads();  // Y_ij is read by the next sub-block of this column
+    }
+}
+
+template <typename T, int IB>
 constexpr size_t inv_offdiag_smem() {
     return sizeof(T) * (2 * L2Cfg<T, IB>::kKC * IB + 2 * IB * (IB + 1));
 }
@@ -198,11 +209,16 @@ constexpr size_t inv_offdiag_smem() {
 // row tile stops at the tile's last row.  256 threads, a TM x TN register
 // patch per thread, double-buffered cp.async staging of BK-deep slabs.
 // ---------------------------------------------------------------------------
-template <typename T> struct GemmCfg;
-template <> struct GemmCfg<float>   { static constexpr int BM = 128, BN = 128, BK = 16, TM = 8, TN = 8; };
-template <> struct GemmCfg<double>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
-template <> struct GemmCfg<float2>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
-template <> struct GemmCfg<double2> { static constexpr int BM = 64,  BN = 32,  BK = 8,  TM = 4, TN = 2; };
+template <typename T, bool SMALL> struct GemmCfg;
+template <> struct GemmCfg<float, false>   { static constexpr int BM = 128, BN = 128, BK = 16, TM = 8, TN = 8; };
+template <> struct GemmCfg<double, false>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
+template <> struct GemmCfg<float2, false>  { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
+template <> struct GemmCfg<double2, false> { static constexpr int BM = 64,  BN = 32,  BK = 8,  TM = 4, TN = 2; };
+// small tiles: 4x more CTAs for grids below two waves
+template <> struct GemmCfg<float, true>    { static constexpr int BM = 64,  BN = 64,  BK = 16, TM = 4, TN = 4; };
+template <> struct GemmCfg<double, true>   { static constexpr int BM = 32,  BN = 32,  BK = 16, TM = 2, TN = 2; };
+template <> struct GemmCfg<float2, true>   { static constexpr int BM = 32,  BN = 32,  BK = 16, TM = 2, TN = 2; };
+template <> struct GemmCfg<double2, true>  { static constexpr int BM = 32,  BN = 16,  BK = 8,  TM = 2, TN = 1; };
 
 template <typename T>
 struct GemmArgs {
@@ -219,9 +235,9 @@ struct GemmArgs {
     int c_rowmajor;  // C element (r, c) at r*ldc + c instead of c*ldc + r
 };
 
-template <typename T>
+template <typename T, bool SMALL>
 __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
-    using C = GemmCfg<T>;
+    using C = GemmCfg<T, SMALL>;
     constexpr int BM = C::BM, BN = C::BN, BK = C::BK, TM = C::TM, TN = C::TN;
     constexpr int NT = (BM / TM) * (BN / TN);
     static_assert(NT == 256, "gemm threads");

@@ -9,13 +9,56 @@
 
 namespace trsm {
 
+// Generic GEMM: the regular tiles when they fill two waves of SMs, else
+// the small tiles.
 template <typename T>
 static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
-    using C = GemmCfg<T>;
+    using C = GemmCfg<T, false>;
+    using S = GemmCfg<T, true>;
     if (g.M <= 0 || g.N <= 0) return TRSM_SUCCESS;
-    const dim3 grid((unsigned)((g.M + C::BM - 1) / C::BM), (unsigned)((g.N + C::BN - 1) / C::BN));
-    gemm_kernel<T><<<grid, 256, 0, st>>>(g);
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+    }
+    const int64_t ctas = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
+    if (ctas >= 2 * sms) {
+        const dim3 grid((unsigned)((g.M + C::BM - 1) / C::BM), (unsigned)((g.N + C::BN - 1) / C::BN));
+        gemm_kernel<T, false><<<grid, 256, 0, st>>>(g);
+    } else {
+        const dim3 grid((unsigned)((g.M + S::BM - 1) / S::BM), (unsigned)((g.N + S::BN - 1) / S::BN));
+        gemm_kernel<T, true><<<grid, 256, 0, st>>>(g);
+    }
     return launch_status();
+}
+
+// Launch the single-precision GEMM with large tiles when they fill at least
+// two waves of the GPU's SMs, else with the small tiles.
+template <typename T>
+static int sp_launch(const SpArgs &g, cudaStream_t st) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+    }
+    using Big = SpTile<T, false>;
+    const int64_t big_ctas = ((g.M + Big::BM - 1) / Big::BM) * ((g.N + Big::BN - 1) / Big::BN);
+    auto go = [&](auto tile_tag, auto kern) -> int {
+        using Tl = decltype(tile_tag);
+        if (Tl::SMEM > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        const dim3 grid((unsigned)((g.M + Tl::BM - 1) / Tl::BM), (unsigned)((g.N + Tl::BN - 1) / Tl::BN));
+        kern<<<grid, 256, Tl::SMEM, st>>>(g);
+        return launch_status();
+    };
+    if (big_ctas >= 2 * sms) return go(SpTile<T, false>{}, sp_update_kernel<T, false>);
+    return go(SpTile<T, true>{}, sp_update_kernel<T, true>);
 }
 
 // Trailing update C = beta*C - A X (A column-major, X row-major panel).
@@ -24,9 +67,8 @@ static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t ld
                          T *C, int64_t ldc, T beta, T minus_one, cudaStream_t st) {
     if (M <= 0 || N <= 0) return TRSM_SUCCESS;
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
-        using Tl = SpTile<T>;
         const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
-                             ((lda * (int64_t)sizeof(T)) % 16 == 0) && (K % Tl::BK == 0);
+                             ((lda * (int64_t)sizeof(T)) % 16 == 0);
         if (aligned) {
             SpArgs g;
             g.M = M; g.N = N; g.K = K;
@@ -39,15 +81,7 @@ static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t ld
             memcpy(&g.gamma, &minus_one, sizeof(T));
             g.beta_zero = 0;
             g.k_by_col = 0;
-            auto kern = sp_update_kernel<T>;
-            if (Tl::SMEM > 48 * 1024) {
-                const cudaError_t e =
-                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
-                if (e != cudaSuccess) return cuda_status(e);
-            }
-            const dim3 grid((unsigned)((M + Tl::BM - 1) / Tl::BM), (unsigned)((N + Tl::BN - 1) / Tl::BN));
-            kern<<<grid, 256, Tl::SMEM, st>>>(g);
-            return launch_status();
+            return sp_launch<T>(g, st);
         }
     }
     GemmArgs<T> up;
@@ -75,7 +109,6 @@ template <typename T>
 static int apply_sp_launch(int64_t mb, int64_t n, const T *Wt, int64_t nb, const T *P, int64_t ldx, T *Xw, T gamma,
                            cudaStream_t st) {
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
-        using Tl = SpTile<T>;
         if (((reinterpret_cast<uintptr_t>(Wt) | reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(Xw)) &
              15) != 0 || (nb * (int64_t)sizeof(T)) % 16 || (ldx * (int64_t)sizeof(T)) % 16)
             return kSpNotApplicable;
@@ -89,14 +122,7 @@ static int apply_sp_launch(int64_t mb, int64_t n, const T *Wt, int64_t nb, const
         memcpy(&g.gamma, &gamma, sizeof(T));
         g.beta_zero = 1;
         g.k_by_col = 1;
-        auto kern = sp_update_kernel<T>;
-        if (Tl::SMEM > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
-            if (e != cudaSuccess) return cuda_status(e);
-        }
-        const dim3 grid((unsigned)((n + Tl::BM - 1) / Tl::BM), (unsigned)((mb + Tl::BN - 1) / Tl::BN));
-        kern<<<grid, 256, Tl::SMEM, st>>>(g);
-        return launch_status();
+        return sp_launch<T>(g, st);
     } else {
         (void)mb; (void)n; (void)Wt; (void)nb; (void)P; (void)ldx; (void)Xw; (void)gamma; (void)st;
         return kSpNotApplicable;
@@ -115,12 +141,8 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    for (int d = 1; d < 8; ++d) {
-        kern<<<dim3(tb, 8 - d), 256, smem, st>>>(L, lda, m, nb, W, d);
-        rc = launch_status();
-        if (rc) return rc;
-    }
-    return TRSM_SUCCESS;
+    kern<<<dim3(tb, 7), 256, smem, st>>>(L, lda, m, nb, W);
+    return launch_status();
 }
 
 struct PhaseTimer {

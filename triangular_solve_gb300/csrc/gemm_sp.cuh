@@ -18,21 +18,35 @@
 
 namespace trsm {
 
-template <typename E> struct SpCfg;
-template <> struct SpCfg<float> {
+// Per-thread tiles.  The large tiles (CTA 128 x 128 for f32, 128 x 64 for
+// complex64) are used when they give at least two waves of CTAs; smaller
+// problems (the last block rows, and m of a few thousand) take the SMALL
+// tiles (64 x 64 / 64 x 32) so that every SM gets work.
+template <typename E, bool SMALL> struct SpCfg;
+template <> struct SpCfg<float, false> {
     static constexpr int VE = 4;            // elements per 16-byte chunk
     static constexpr int RM = 8, RN = 8;    // per-thread tile
     static constexpr int BK = 16, STAGES = 4;
 };
-template <> struct SpCfg<float2> {
+template <> struct SpCfg<float, true> {
+    static constexpr int VE = 4;
+    static constexpr int RM = 4, RN = 4;
+    static constexpr int BK = 16, STAGES = 4;
+};
+template <> struct SpCfg<float2, false> {
     static constexpr int VE = 2;
     static constexpr int RM = 8, RN = 4;
     static constexpr int BK = 16, STAGES = 3;
 };
+template <> struct SpCfg<float2, true> {
+    static constexpr int VE = 2;
+    static constexpr int RM = 4, RN = 2;
+    static constexpr int BK = 16, STAGES = 4;
+};
 
-template <typename E>
+template <typename E, bool SMALL = false>
 struct SpTile {
-    using C = SpCfg<E>;
+    using C = SpCfg<E, SMALL>;
     static constexpr int VE = C::VE, RM = C::RM, RN = C::RN, BK = C::BK, STAGES = C::STAGES;
     static constexpr int WM = 8 * RM, WN = 4 * RN;   // warp tile (lanes 8 x 4)
     static constexpr int BM = 2 * WM, BN = 4 * WN;   // CTA tile (warps 2 x 4)
@@ -116,9 +130,9 @@ struct AccTile<float2, RM, RN> {
     __device__ __forceinline__ float2 get(int i, int j) const { return v[i][j]; }
 };
 
-template <typename E>
+template <typename E, bool SMALL>
 __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
-    using Tl = SpTile<E>;
+    using Tl = SpTile<E, SMALL>;
     constexpr int VE = Tl::VE, RM = Tl::RM, RN = Tl::RN, BK = Tl::BK, STAGES = Tl::STAGES;
     constexpr int BM = Tl::BM, BN = Tl::BN;
     extern __shared__ __align__(16) unsigned char smem_raw[];

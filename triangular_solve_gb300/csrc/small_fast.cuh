@@ -13,7 +13,6 @@
 //  * X goes from registers straight to global memory with 16-byte stores.
 #pragma once
 
-#include <stdlib.h>
 #include <string.h>
 
 #include <type_traits>
@@ -22,16 +21,6 @@
 #include "small_kernels.cuh"
 
 namespace trsm {
-
-// Which f32 small kernel serves n > 32 (set once from TRSM_F32_SMALL: 0 =
-// column pipeline, 1 = two-dimensional tiles).
-inline int trsm_f32_small_variant() {
-    static const int v = [] {
-        const char *e = getenv("TRSM_F32_SMALL");
-        return e ? atoi(e) : 1;
-    }();
-    return v;
-}
 
 template <typename T, int M, int W>
 struct FastImage {
@@ -480,166 +469,6 @@ __global__ void __launch_bounds__(64 * kPipePairs, 1) small_pipe_f32_kernel(cons
     cp_async_wait_all();
 }
 
-// ---------------------------------------------------------------------------
-// f32 two-dimensional register tiles.  One warp per work item (system,
-// 64-column slice).  Lane (rg, cg) = (lane / 16, lane % 16) owns the row
-// quads q = 2j + rg (j < M/8) -- rows interleaved four at a time so that all
-// lanes stay busy to the end of the triangle -- of columns 4cg .. 4cg+3, as
-// packed row pairs (128 registers at M = 64).  Step kq handles the four rows
-// of quad kq: the 16 lanes owning it solve the 4 x 4 diagonal block for
-// their columns and publish -x through a double-buffered shared line; then
-// every lane updates its quads below kq with the four columns of L, one
-// 16-byte load of L per quad and column feeding eight paired FMAs.  Versus a
-// thread per column this needs about four times fewer shared-memory
-// wavefronts per system, the resource that bounds the column kernels.
-// ---------------------------------------------------------------------------
-template <int M>
-struct QuadImage {
-    static constexpr int kLs = Packed<float, M>::kSize;
-    static constexpr int kX = kLs + M;              // -x lines: [2][4 rows][64 columns]
-    static constexpr int kElems = kX + 2 * 4 * 64;
-    static constexpr int kChunks = kLs / 4;
-    static_assert(kElems % 4 == 0, "16-byte aligned images");
-};
-
-template <int M, int KQ>
-struct QuadSteps {
-    static __device__ __forceinline__ void run(const float *__restrict__ Ls, float *__restrict__ xs, int rg, int cg,
-                                               f32x2 (&acc)[M / 8][2][4]) {
-        if constexpr (KQ < M / 4) {
-            using P = Packed<float, M>;
-            constexpr int k = 4 * KQ;
-            constexpr int JO = KQ / 2;  // owner's quad slot
-            const float *dinv = Ls + QuadImage<M>::kLs;
-            float *xl = xs + (KQ & 1) * 256;  // this step's -x line: [4 rows][64 columns]
-            if (rg == (KQ & 1)) {
-                const float d0 = dinv[k], d1 = dinv[k + 1], d2 = dinv[k + 2], d3 = dinv[k + 3];
-                const float l10 = P::col(Ls, k)[k + 1], l20 = P::col(Ls, k)[k + 2], l30 = P::col(Ls, k)[k + 3];
-                const float l21 = P::col(Ls, k + 1)[k + 2], l31 = P::col(Ls, k + 1)[k + 3];
-                const float l32 = P::col(Ls, k + 2)[k + 3];
-                float4 n0, n1, n2, n3;
-                float *n0p = &n0.x, *n1p = &n1.x, *n2p = &n2.x, *n3p = &n3.x;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float b0, b1, b2, b3;
-                    unpack2(acc[JO][0][c], b0, b1);
-                    unpack2(acc[JO][1][c], b2, b3);
-                    const float x0 = b0 * d0;
-                    const float x1 = fmaf(-l10, x0, b1) * d1;
-                    const float x2 = fmaf(-l21, x1, fmaf(-l20, x0, b2)) * d2;
-                    const float x3 = fmaf(-l32, x2, fmaf(-l31, x1, fmaf(-l30, x0, b3))) * d3;
-                    acc[JO][0][c] = pack2(x0, x1);
-                    acc[JO][1][c] = pack2(x2, x3);
-                    n0p[c] = -x0;
-                    n1p[c] = -x1;
-                    n2p[c] = -x2;
-                    n3p[c] = -x3;
-                }
-                *reinterpret_cast<float4 *>(xl + 0 * 64 + 4 * cg) = n0;
-                *reinterpret_cast<float4 *>(xl + 1 * 64 + 4 * cg) = n1;
-                *reinterpret_cast<float4 *>(xl + 2 * 64 + 4 * cg) = n2;
-                *reinterpret_cast<float4 *>(xl + 3 * 64 + 4 * cg) = n3;
-            }
-            __syncwarp();
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 nv = *reinterpret_cast<const float4 *>(xl + r * 64 + 4 * cg);
-                const f32x2 nx[4] = {pack2(nv.x, nv.x), pack2(nv.y, nv.y), pack2(nv.z, nv.z), pack2(nv.w, nv.w)};
-                const float *col = P::col(Ls, k + r);
-#pragma unroll
-                for (int j = 0; j < M / 8; ++j) {
-                    // quad 2j + rg is below quad KQ for every lane when 2j > KQ,
-                    // for no lane when 2j + 1 <= KQ, for rg = 1 when 2j == KQ
-                    if (2 * j + 1 <= KQ) continue;
-                    if (2 * j == KQ && rg == 0) continue;
-                    const ulonglong2 l = *reinterpret_cast<const ulonglong2 *>(col + 4 * (2 * j + rg));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        acc[j][0][c] = ffma2(l.x, nx[c], acc[j][0][c]);
-                        acc[j][1][c] = ffma2(l.y, nx[c], acc[j][1][c]);
-                    }
-                }
-            }
-            QuadSteps<M, KQ + 1>::run(Ls, xs, rg, cg, acc);
-        }
-    }
-};
-
-constexpr int kQuadWarps = 4;
-
-template <int M>
-__global__ void __launch_bounds__(32 * kQuadWarps, M >= 64 ? 2 : 3) small_quad_f32_kernel(const SmallGeom g, const float alpha,
-                                                                          const int64_t items) {
-    using Img = QuadImage<M>;
-    using P = Packed<float, M>;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *images = reinterpret_cast<float *>(smem_raw);
-    ChunkEntry *tab = reinterpret_cast<ChunkEntry *>(images + kQuadWarps * Img::kElems);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int k = tid; k < M; k += blockDim.x) {
-        const int nch = (M - P::s(k)) / 4;
-        const int first = P::off(k) / 4;
-        for (int q = 0; q < nch; ++q) {
-            ChunkEntry e;
-            e.k = (unsigned short)k;
-            e.row0 = (unsigned short)(P::s(k) + 4 * q);
-            e.dst = (unsigned short)(P::off(k) + 4 * q);
-            tab[first + q] = e;
-        }
-    }
-    __syncthreads();
-    const int64_t item = (int64_t)blockIdx.x * kQuadWarps + warp;
-    if (item >= items) return;  // warp-uniform; no CTA barrier follows
-    const int slices = (g.n + 63) / 64;
-    const int64_t sys = item / slices;
-    const int j0 = (int)(item - sys * slices) * 64;
-    const int rg = lane >> 4, cg = lane & 15;
-    float *img = images + warp * Img::kElems;
-    const float *A = static_cast<const float *>(g.A) + sys * g.sA;
-    float *B = static_cast<float *>(g.B) + sys * g.sB;
-
-    for (int e = lane; e < Img::kChunks; e += 32) {
-        const ChunkEntry c = tab[e];
-        cp_async<16>(img + c.dst, A + (int64_t)c.k * g.lda + c.row0);
-    }
-    cp_async_commit();
-    // the lane's tile straight into packed row pairs
-    f32x2 acc[M / 8][2][4];
-    float *gcol[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int j = j0 + 4 * cg + c;
-        gcol[c] = j < g.n ? B + (int64_t)j * g.ldb : nullptr;
-#pragma unroll
-        for (int jq = 0; jq < M / 8; ++jq) {
-            ulonglong2 v = make_ulonglong2(0ull, 0ull);
-            if (gcol[c]) v = *reinterpret_cast<const ulonglong2 *>(gcol[c] + 4 * (2 * jq + rg));
-            acc[jq][0][c] = v.x;
-            acc[jq][1][c] = v.y;
-        }
-    }
-    cp_async_wait_all();
-    __syncwarp();
-    for (int k = lane; k < M; k += 32) img[Img::kLs + k] = 1.0f / img[P::off(k) + (k - P::s(k))];
-    __syncwarp();
-    const f32x2 a2 = pack2(alpha, alpha);
-#pragma unroll
-    for (int jq = 0; jq < M / 8; ++jq)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            acc[jq][0][c] = ffma2(a2, acc[jq][0][c], 0ull);
-            acc[jq][1][c] = ffma2(a2, acc[jq][1][c], 0ull);
-        }
-    QuadSteps<M, 0>::run(img, img + Img::kX, rg, cg, acc);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (gcol[c] == nullptr) continue;
-#pragma unroll
-        for (int jq = 0; jq < M / 8; ++jq)
-            *reinterpret_cast<ulonglong2 *>(gcol[c] + 4 * (2 * jq + rg)) = make_ulonglong2(acc[jq][0][c], acc[jq][1][c]);
-    }
-}
-
 // CTA: SPC systems x (W / CPT) threads each.  Thread g of a system owns
 // columns g + c*(W/CPT), c < CPT, of the CTA's column slice.
 template <typename T, int M, int W, int CPT, int RC, int SPC>
@@ -765,27 +594,9 @@ static int launch_pipe_f32(const SmallGeom &g, float alpha, cudaStream_t st) {
     return launch_status();
 }
 
-template <int M>
-static int launch_quad_f32(const SmallGeom &g, float alpha, cudaStream_t st) {
-    using Img = QuadImage<M>;
-    constexpr size_t smem = (size_t)kQuadWarps * Img::kElems * sizeof(float) + Img::kChunks * sizeof(ChunkEntry);
-    auto kern = small_quad_f32_kernel<M>;
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    const int64_t items = g.batch * ((g.n + 63) / 64);
-    const int64_t ctas = (items + kQuadWarps - 1) / kQuadWarps;
-    kern<<<(unsigned)ctas, 32 * kQuadWarps, smem, st>>>(g, alpha, items);
-    return launch_status();
-}
-
 template <typename T, int M>
 static int launch_fast_m(const SmallGeom &g, T alpha, cudaStream_t st) {
     if constexpr (std::is_same<T, float>::value) {
-        if constexpr (M >= 16) {
-            if (g.n > 32 && trsm_f32_small_variant() == 1) return launch_quad_f32<M>(g, alpha, st);
-        }
         if (g.n <= 32) return launch_reg_f32<M, 32>(g, alpha, st);
         if constexpr (M >= 16) {
             // many items: the persistent pipelined kernel; a handful: one CTA
