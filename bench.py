@@ -43,6 +43,13 @@ import trsm_inputs as ti  # noqa: E402
 DTYPES = ("f32", "f64", "c64", "c128")
 TORCH_NAME = {"f32": "float32", "f64": "float64", "c64": "complex64", "c128": "complex128"}
 SQUARE = dict(m=64, n=64, batch=4096)
+# the kernel that solves the square64 batch of each type, and its key in
+# profiles/traffic.json
+SQUARE_KERNEL = {"f32": "small_pipe_f32_kernel<64>", "f64": "small_fast_kernel<double, 64, 64, 1, 64, 2>",
+                 "c64": "small_fast_kernel<float2, 64, 64, 1, 64, 2>",
+                 "c128": "small_fast_kernel<double2, 64, 64, 1, 32, 2>"}
+SQUARE_TRAFFIC_KEY = {"f32": "small_pipe_f32_kernel", "f64": "small_fast_kernel<f64>",
+                      "c64": "small_fast_kernel<c64>", "c128": "small_fast_kernel<c128>"}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
 FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike)
 SM_COUNT, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
@@ -321,8 +328,10 @@ def run_gb300(args, ws, rank, local):
         roof = {"bound": "hbm", "achieved": ti.algorithmic_bytes(dom, m, n, batch) / (dom_ms * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_source": f"hbm_gbs ({peak_src})"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = f"small_colreg_kernel<{dom}, 64> (square64 batch 4096)"
-    roof["traffic"] = recorded_traffic(f"small_colreg/{dom}/square64x4096")
+    roof["kernel"] = f"{SQUARE_KERNEL[dom]} (square64, batch 4096)"
+    roof["algorithmic_per_launch"] = (ti.flops(dom, m, n, batch) if roof["bound"] == "alu"
+                                      else ti.algorithmic_bytes(dom, m, n, batch))
+    roof["traffic"] = recorded_traffic(f"{SQUARE_TRAFFIC_KEY[dom]}/square64x4096")
     roof["achieved"] = round(roof["achieved"], 3)
     roof["frac"] = round(roof["frac"], 4)
 
