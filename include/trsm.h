@@ -57,6 +57,7 @@ typedef enum { TRSM_COL_MAJOR = 0, TRSM_ROW_MAJOR = 1 } trsm_layout_t;
 
 #define TRSM_SUCCESS 0
 #define TRSM_ERR_WORKSPACE 900      /* caller workspace too small or misaligned */
+#define TRSM_ERR_DEVICE_TIMEOUT 901 /* a kernel's bounded wait expired (see trsm_device_status) */
 #define TRSM_ERR_CUDA_BASE 1000     /* TRSM_ERR_CUDA_BASE + cudaError_t */
 
 /*
@@ -178,6 +179,17 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
  */
 int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
                       const void *A, int64_t lda, void *B, int64_t ldb, void *stream);
+
+/*
+ * Device-side status of the current device: the kernels that wait on
+ * hardware barriers (the tensor-core update of the f32 blocked path) bound
+ * every wait; when one expires the kernel abandons its tile and records
+ * TRSM_ERR_DEVICE_TIMEOUT here instead of hanging.  Synchronises the current
+ * device, returns TRSM_SUCCESS or TRSM_ERR_DEVICE_TIMEOUT (or a CUDA error
+ * status), and resets the word to TRSM_SUCCESS when `clear` is non-zero.
+ * No counterpart on the pages.
+ */
+int trsm_device_status(int clear);
 
 /* Static, human-readable text for a status code returned by this library. */
 const char *trsm_status_string(int status);

@@ -20,7 +20,8 @@ import threading
 
 __all__ = [
     "trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_select_nb", "trsm_llnn_workspace_bytes",
-    "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string", "solve", "TrsmError",
+    "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string", "trsm_llnn_noalloc", "trsm_device_status",
+    "solve", "TrsmError",
     "library_path", "load_library",
 ]
 
@@ -205,6 +206,16 @@ def trsm_llnn_noalloc(dtype, m, n, alpha, A, lda, B, ldb, stream=None) -> None:
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+ERR_DEVICE_TIMEOUT = 901
+
+
+def trsm_device_status(clear: bool = True) -> int:
+    """Device-side status (0, or 901 when a kernel's bounded wait expired);
+    synchronises the current device."""
+    fn = load_library().trsm_device_status
+    fn.argtypes = [ctypes.c_int]
+    fn.restype = ctypes.c_int
+    return int(fn(1 if clear else 0))
 
 
 def trsm_status_string(status: int) -> str:

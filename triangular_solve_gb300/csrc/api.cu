@@ -303,10 +303,13 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
     return rc;
 }
 
+int trsm_device_status(int clear) { return device_status(clear); }
+
 const char *trsm_status_string(int status) {
     if (status == TRSM_SUCCESS) return "success";
     if (status < 0) return "invalid argument (the negated status is its 1-based position)";
     if (status == TRSM_ERR_WORKSPACE) return "workspace missing, misaligned or too small";
+    if (status == TRSM_ERR_DEVICE_TIMEOUT) return "a kernel's bounded wait on a hardware barrier expired";
     if (status >= TRSM_ERR_CUDA_BASE) return cudaGetErrorString((cudaError_t)(status - TRSM_ERR_CUDA_BASE));
     return "unknown status";
 }

@@ -64,8 +64,13 @@ static int sp_launch(const SpArgs &g, cudaStream_t st) {
 // Trailing update C = beta*C - A X (A column-major, X row-major panel).
 template <typename T>
 static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t lda, const T *X, int64_t ldx,
-                         T *C, int64_t ldc, T beta, T minus_one, cudaStream_t st) {
+                         T *C, int64_t ldc, T beta, T minus_one, cudaStream_t st, int64_t Mmax = 0,
+                         void *tc_panels = nullptr) {
     if (M <= 0 || N <= 0) return TRSM_SUCCESS;
+    if constexpr (std::is_same<T, float>::value) {
+        if (tc_panels && tc_update_usable(M, N, K))
+            return tc_update_f32(M, N, K, A, lda, X, ldx, C, ldc, beta, Mmax, tc_panels, st);
+    }
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
         const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
                              ((lda * (int64_t)sizeof(T)) % 16 == 0);
@@ -188,6 +193,9 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     T *W = static_cast<T *>(a.ws);
     T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + round256(tbk * nb * nb * (int64_t)sizeof(T)));
     T *Pw = reinterpret_cast<T *>(reinterpret_cast<char *>(Xw) + round256(nb * ldx * (int64_t)sizeof(T)));
+    void *tc_panels = nullptr;
+    if constexpr (std::is_same<T, float>::value)
+        tc_panels = reinterpret_cast<char *>(Pw) + round256(nb * ldx * (int64_t)sizeof(T));
 
     PhaseTimer timer;
     int rc = TRSM_SUCCESS;
@@ -247,7 +255,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
             const T beta = (t == 0) ? alpha : one;
             const T *Lp = L + r0 * a.lda + r0 + nb;
             if ((rc = update_launch<T>(m - r0 - nb, n, nb, Lp, a.lda, Xw, ldx, B + r0 + nb, a.ldb, beta,
-                                       minus_one, st)))
+                                       minus_one, st, m, tc_panels)))
                 return rc;
         }
         {

@@ -63,10 +63,22 @@ struct BlockedArgs {
 // rounded up to 256 bytes.
 inline int64_t panel_ld(int64_t n) { return ((n > 0 ? n : 1) + 3) / 4 * 4; }
 inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+// f32 adds the TF32 head/tail panels of the tensor-core update
+// (tc_panel_bytes: L panel and X_t panel, two copies each, K-major).
+size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb);
 inline size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb) {
     const int64_t tb = (m + nb - 1) / nb;
-    return (size_t)(round256(tb * nb * nb * elem_bytes) + 2 * round256(nb * panel_ld(n) * elem_bytes));
+    size_t b = (size_t)(round256(tb * nb * nb * elem_bytes) + 2 * round256(nb * panel_ld(n) * elem_bytes));
+    if (elem_bytes == 4) b += tc_panel_bytes(m, n, nb);
+    return b;
 }
+
+// Tensor-core (tcgen05, 3xTF32) f32 trailing update; see tc_gemm.cuh.
+bool tc_update_usable(int64_t M, int64_t N, int64_t K);
+int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
+                  float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st);
+// Device status word of the bounded waits (synchronises the device).
+int device_status(int clear);
 
 int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);
 int blocked_solve_f64(const BlockedArgs &a, cudaStream_t st);

@@ -1,0 +1,139 @@
+// Host side of the tensor-core f32 trailing update: TF32 head/tail split of
+// the two panels, tensor maps for the TMA loads, launch, and the device
+// status word that the kernels' bounded waits report to.
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "tc_gemm.cuh"
+
+namespace trsm {
+
+namespace {
+
+static __device__ int g_device_status;  // TRSM_ERR_DEVICE_TIMEOUT when a bounded wait expired
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDev] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int status_word(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDev) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return TRSM_SUCCESS;
+}
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000 *out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (q != cudaDriverEntryPointSuccess || !fn) return TRSM_ERR_CUDA_BASE + (int)cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return TRSM_SUCCESS;
+}
+
+// K-major rows x k matrix (row stride ld floats), box 32 (k) x box_rows.
+int make_map(CUtensorMap *map, const float *p, int64_t rows, int64_t k, int64_t ld, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = encoder(&enc);
+    if (rc) return rc;
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * (int64_t)sizeof(float))};
+    const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TRSM_SUCCESS : TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
+}
+
+int split(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, float *lo, int64_t ldd, cudaStream_t st) {
+    const dim3 grid((unsigned)((R + 31) / 32), (unsigned)((Kc + 31) / 32));
+    split_tf32_kernel<<<grid, dim3(32, 8), 0, st>>>(src, ks, R, Kc, hi, lo, ldd);
+    return launch_status();
+}
+
+}  // namespace
+
+size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb) {
+    return (size_t)(2 * round256(m * nb * 4) + 2 * round256(n * nb * 4));
+}
+
+bool tc_update_usable(int64_t M, int64_t N, int64_t K) {
+    // boxes never larger than the tensors they read
+    return M >= TC_BM && N >= TC_BN && K >= TC_BK && K % TC_BK == 0;
+}
+
+// C (M x N, column-major ldc) = beta*C - L_panel (M x K, column-major lda) *
+// X (K x N, row-major ldx), through TF32 head/tail panels in `panels`
+// (tc_panel_bytes(Mmax, N, K) bytes, 256-byte aligned).
+int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
+                  float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st) {
+    float *a_hi = static_cast<float *>(panels);
+    float *a_lo = reinterpret_cast<float *>(reinterpret_cast<char *>(a_hi) + round256(Mmax * K * 4));
+    float *x_hi = reinterpret_cast<float *>(reinterpret_cast<char *>(a_lo) + round256(Mmax * K * 4));
+    float *x_lo = reinterpret_cast<float *>(reinterpret_cast<char *>(x_hi) + round256(N * K * 4));
+    int rc = split(A, lda, M, K, a_hi, a_lo, K, st);         // L panel rows, K-major
+    if (!rc) rc = split(X, ldx, N, K, x_hi, x_lo, K, st);    // X_t columns, K-major
+    if (rc) return rc;
+    CUtensorMap ma_hi, ma_lo, mx_hi, mx_lo;
+    if ((rc = make_map(&ma_hi, a_hi, M, K, K, TC_BM))) return rc;
+    if ((rc = make_map(&ma_lo, a_lo, M, K, K, TC_BM))) return rc;
+    if ((rc = make_map(&mx_hi, x_hi, N, K, K, TC_BN))) return rc;
+    if ((rc = make_map(&mx_lo, x_lo, N, K, K, TC_BN))) return rc;
+    int *status = nullptr;
+    if ((rc = status_word(&status))) return rc;
+    TcArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.C = C;
+    g.ldc = ldc;
+    g.beta = beta;
+    g.status = status;
+    const cudaError_t e =
+        cudaFuncSetAttribute(tc_update_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return cuda_status(e);
+    const dim3 grid((unsigned)((M + TC_BM - 1) / TC_BM), (unsigned)((N + TC_BN - 1) / TC_BN));
+    tc_update_f32_kernel<<<grid, 192, TC_SMEM, st>>>(ma_hi, ma_lo, mx_hi, mx_lo, g);
+    return launch_status();
+}
+
+int device_status(int clear) {
+    int *p = nullptr;
+    int rc = status_word(&p);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_status(e);
+    int v = 0;
+    e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (clear && v) {
+        const int z = 0;
+        e = cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return v;
+}
+
+}  // namespace trsm

@@ -1,0 +1,304 @@
+// Trailing-update GEMM for f32 on the fifth-generation tensor cores
+// (tcgen05, sm_100 family):  C = beta*C - A * X
+// with A (M x K) the L panel and X (K x N) the X_t panel, K = NB.
+//
+// f32 accuracy from TF32 tensor cores: each operand is split into a TF32
+// head and a TF32 tail (a = hi + lo, hi = tf32(a), lo = tf32(a - hi)) by a
+// preprocessing pass, and the product is accumulated in FP32 as
+//     A_hi X_hi + A_hi X_lo + A_lo X_hi
+// (the dropped A_lo X_lo term is ~2^-22 relative).  The operands are stored
+// K-major (row-major panels), the layout the tensor-core descriptors read.
+//
+// One CTA computes a 128 x 256 tile with six warps:
+//   warp 0  TMA producer: 2-D tensor loads of the four operand tiles of a
+//           32-deep K slab into a two-stage shared-memory ring (128-byte
+//           swizzle), completion counted on the stage's "full" mbarrier;
+//   warp 1  MMA issuer: one elected thread issues tcgen05.mma (kind::tf32,
+//           M = 128, N = 256, K = 8) into an FP32 accumulator in tensor
+//           memory (256 columns), and tcgen05.commit frees each stage and
+//           finally signals the epilogue;
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, then
+//           C = beta*C - acc straight to global memory (coalesced per column).
+// Every mbarrier wait is bounded: when a wait expires the kernel records
+// TRSM_ERR_DEVICE_TIMEOUT in a device status word and the CTA unwinds
+// (no hang), releasing its tensor memory.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace trsm {
+
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 32, TC_STAGES = 2;
+constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 16 KB
+constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 32 KB
+constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 96 KB
+constexpr uint32_t TC_TMEM_COLS = 256;
+constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
+constexpr uint32_t TC_WAIT_LIMIT = 1u << 24;  // try_wait rounds before giving up
+
+struct TcArgs {
+    int64_t M, N, K;
+    float *C;
+    int64_t ldc;
+    float beta;
+    int *status;  // device status word (0 = ok)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false when it expired.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < TC_WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
+// rows of 128 bytes (32 TF32 values), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                   // leading byte offset (unused when swizzled)
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                   // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::tf32, FP32 accumulator, A and B K-major.
+__host__ __device__ constexpr uint32_t tf32_idesc(int m, int n) {
+    return (1u << 4)                     // D format F32
+           | (2u << 7)                   // A format TF32
+           | (2u << 10)                  // B format TF32
+           | ((uint32_t)(n >> 3) << 17)  // N / 8
+           | ((uint32_t)(m >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void record_timeout(int *status) {
+    if (status) atomicExch(status, TRSM_ERR_DEVICE_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(192, 1)
+    tc_update_f32_kernel(const __grid_constant__ CUtensorMap mA_hi, const __grid_constant__ CUtensorMap mA_lo,
+                         const __grid_constant__ CUtensorMap mX_hi, const __grid_constant__ CUtensorMap mX_lo,
+                         const TcArgs g) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *sbase = smem_raw + (base - raw);
+    const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;  // full[2], empty[2], done, tmem slot
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 16u + 8u * s; };
+    const uint32_t done_bar = bars + 32u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + 40);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * TC_BM, n0 = blockIdx.y * TC_BN;
+    const int nk = (int)((g.K + TC_BK - 1) / TC_BK);
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % TC_STAGES;
+                if (kb >= TC_STAGES && !mbar_wait(empty(s), ((kb / TC_STAGES) - 1) & 1)) {
+                    record_timeout(g.status);
+                    abort_flag = 1;
+                    break;
+                }
+                if (*(volatile int *)&abort_flag) break;
+                const uint32_t st = base + s * TC_STAGE_BYTES;
+                mbar_expect_tx(full(s), TC_STAGE_BYTES);
+                const int kx = kb * TC_BK;
+                tma_load_2d(st, &mA_hi, kx, m0, full(s));
+                tma_load_2d(st + TC_A_BYTES, &mA_lo, kx, m0, full(s));
+                tma_load_2d(st + 2 * TC_A_BYTES, &mX_hi, kx, n0, full(s));
+                tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &mX_lo, kx, n0, full(s));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tf32_idesc(TC_BM, TC_BN);
+            bool ok = true;
+            for (int kb = 0; kb < nk && ok; ++kb) {
+                const int s = kb % TC_STAGES;
+                if (!mbar_wait(full(s), (kb / TC_STAGES) & 1)) {
+                    record_timeout(g.status);
+                    abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+                const uint32_t st = base + s * TC_STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < TC_BK / 8; ++kk) {
+                    const uint64_t a_hi = sw128_desc(st + kk * 32);
+                    const uint64_t a_lo = sw128_desc(st + TC_A_BYTES + kk * 32);
+                    const uint64_t x_hi = sw128_desc(st + 2 * TC_A_BYTES + kk * 32);
+                    const uint64_t x_lo = sw128_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
+                    mma_tf32(tmem, a_hi, x_hi, idesc, (kb | kk) != 0);
+                    mma_tf32(tmem, a_hi, x_lo, idesc, 1);
+                    mma_tf32(tmem, a_lo, x_hi, idesc, 1);
+                }
+                mma_commit(empty(s));  // the stage is free once these MMAs have read it
+            }
+            mma_commit(done_bar);  // accumulator complete (or abandoned)
+        }
+    } else {
+        // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31.  A thread owns
+        // one row of the tile; C is read a 32-column chunk at a time into
+        // registers (32 loads in flight), the next chunk's loads are issued
+        // before the current chunk is written, and the first chunk is
+        // fetched while the main loop still runs.
+        const int quarter = warp & 3;
+        const int64_t gr = m0 + 32 * quarter + lane;
+        const bool row_ok = gr < g.M;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+        float cnext[32];
+        auto fetch = [&](int chunk, float (&dst)[32]) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int64_t gc = n0 + chunk * 32 + j;
+                dst[j] = (row_ok && gc < g.N) ? g.C[gc * g.ldc + gr] : 0.f;
+            }
+        };
+        fetch(0, cnext);
+        const bool ok = mbar_wait(done_bar, 0);
+        if (!ok) {
+            if (lane == 0) record_timeout(g.status);
+        } else if (!*(volatile int *)&abort_flag) {
+            asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+#pragma unroll 1
+            for (int chunk = 0; chunk < TC_BN / 32; ++chunk) {
+                float ccur[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ccur[j] = cnext[j];
+                if (chunk + 1 < TC_BN / 32) fetch(chunk + 1, cnext);
+                uint32_t v[32];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                    "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                      "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+                      "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+                      "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(lane_addr + (uint32_t)(chunk * 32)));
+                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t gc = n0 + chunk * 32 + j;
+                        if (gc < g.N) g.C[gc * g.ldc + gr] = fmaf(g.beta, ccur[j], -__uint_as_float(v[j]));
+                    }
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TC_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// a = hi + lo with hi, lo both TF32 (round to nearest): dst rows r, K-major,
+//   hi[r * ldd + k] = tf32(src[r + k * ks]),  lo = tf32(src - hi)
+// for r < R, k < Kc.  32 x 32 tiles through shared memory (src is read
+// along r, dst written along k).
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__global__ void split_tf32_kernel(const float *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
+                                  float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    __shared__ float tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + threadIdx.x, k = k0 + q;
+        tile[q][threadIdx.x] = (r < R && k < Kc) ? src[r + k * ks] : 0.f;
+    }
+    __syncthreads();
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + q, k = k0 + threadIdx.x;
+        if (r < R && k < Kc) {
+            const float a = tile[threadIdx.x][q];
+            const float h = to_tf32(a);
+            hi[r * ldd + k] = h;
+            lo[r * ldd + k] = to_tf32(a - h);
+        }
+    }
+}
+
+}  // namespace trsm
