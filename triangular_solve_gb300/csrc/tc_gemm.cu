@@ -114,8 +114,16 @@ int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
     const cudaError_t e =
         cudaFuncSetAttribute(tc_update_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return cuda_status(e);
-    const dim3 grid((unsigned)((M + TC_BM - 1) / TC_BM), (unsigned)((N + TC_BN - 1) / TC_BN));
-    tc_update_f32_kernel<<<grid, 192, TC_SMEM, st>>>(ma_hi, ma_lo, mx_hi, mx_lo, g);
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+    }
+    const int64_t tiles = ((M + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN);
+    const unsigned ctas = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
+    tc_update_f32_kernel<<<ctas, 192, TC_SMEM, st>>>(ma_hi, ma_lo, mx_hi, mx_lo, g);
     return launch_status();
 }
 

@@ -9,19 +9,23 @@
 // (the dropped A_lo X_lo term is ~2^-22 relative).  The operands are stored
 // K-major (row-major panels), the layout the tensor-core descriptors read.
 //
-// One CTA computes a 128 x 256 tile with six warps:
+// Persistent kernel, one CTA per SM, each CTA taking 128 x 256 output tiles
+// in turn, with six warps:
 //   warp 0  TMA producer: 2-D tensor loads of the four operand tiles of a
 //           32-deep K slab into a two-stage shared-memory ring (128-byte
 //           swizzle), completion counted on the stage's "full" mbarrier;
+//           the ring runs on from one tile to the next;
 //   warp 1  MMA issuer: one elected thread issues tcgen05.mma (kind::tf32,
-//           M = 128, N = 256, K = 8) into an FP32 accumulator in tensor
-//           memory (256 columns), and tcgen05.commit frees each stage and
-//           finally signals the epilogue;
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, then
-//           C = beta*C - acc straight to global memory (coalesced per column).
+//           M = 128, N = 256, K = 8) into one of two FP32 accumulators in
+//           tensor memory (2 x 256 columns); tcgen05.commit frees each stage
+//           and signals "accumulator full";
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, release of the
+//           accumulator, then C = beta*C - acc straight to global memory
+//           (coalesced per column) while the MMAs of the next tile run.
 // Every mbarrier wait is bounded: when a wait expires the kernel records
 // TRSM_ERR_DEVICE_TIMEOUT in a device status word and the CTA unwinds
-// (no hang), releasing its tensor memory.
+// (no hang): it waits (bounded) for its TMA loads and MMAs in flight, then
+// releases its tensor memory.
 #pragma once
 
 #include <cuda.h>
@@ -35,7 +39,7 @@ constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 32, TC_STAGES = 2;
 constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 16 KB
 constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 32 KB
 constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 96 KB
-constexpr uint32_t TC_TMEM_COLS = 256;
+constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column FP32 accumulators
 constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
 constexpr uint32_t TC_WAIT_LIMIT = 1u << 24;  // try_wait rounds before giving up
 
@@ -123,25 +127,37 @@ __device__ __forceinline__ void record_timeout(int *status) {
     if (status) atomicExch(status, TRSM_ERR_DEVICE_TIMEOUT);
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Persistent: one CTA per SM walks the output tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  (consecutive CTAs take consecutive row tiles of
+// one column tile, so they share the X_t tile in L2).  The operand ring runs
+// on across tile boundaries, and the accumulator alternates between two
+// 256-column halves of tensor memory: the MMA warp fills one while the
+// epilogue warps drain the other (acc_full / acc_empty barriers).
 __global__ void __launch_bounds__(192, 1)
     tc_update_f32_kernel(const __grid_constant__ CUtensorMap mA_hi, const __grid_constant__ CUtensorMap mA_lo,
                          const __grid_constant__ CUtensorMap mX_hi, const __grid_constant__ CUtensorMap mX_lo,
                          const TcArgs g) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment for the swizzled tiles
     unsigned char *sbase = smem_raw + (base - raw);
-    const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;  // full[2], empty[2], done, tmem slot
+    const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 16u + 8u * s; };
-    const uint32_t done_bar = bars + 32u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + 40);
+    auto acc_full = [&](int a) { return bars + 32u + 8u * a; };
+    auto acc_empty = [&](int a) { return bars + 48u + 8u * a; };
+    const uint32_t drain = bars + 64u;  // last commit of the MMA thread
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + 72);
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * TC_BM, n0 = blockIdx.y * TC_BN;
     const int nk = (int)((g.K + TC_BK - 1) / TC_BK);
+    const int tiles_m = (int)((g.M + TC_BM - 1) / TC_BM);
+    const int ntiles = tiles_m * (int)((g.N + TC_BN - 1) / TC_BN);
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -149,7 +165,11 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(done_bar, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 1) {
@@ -162,78 +182,108 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    auto aborted = [&]() { return *(volatile int *)&abort_flag != 0; };
+    auto fail = [&]() {
+        record_timeout(g.status);
+        abort_flag = 1;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TC_STAGES;
-                if (kb >= TC_STAGES && !mbar_wait(empty(s), ((kb / TC_STAGES) - 1) & 1)) {
-                    record_timeout(g.status);
-                    abort_flag = 1;
-                    break;
+            int it = 0;
+            for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
+                const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % TC_STAGES;
+                    if (it >= TC_STAGES && !mbar_wait(empty(s), ((it / TC_STAGES) - 1) & 1)) {
+                        fail();
+                        break;
+                    }
+                    const uint32_t st = base + s * TC_STAGE_BYTES;
+                    mbar_expect_tx(full(s), TC_STAGE_BYTES);
+                    const int kx = kb * TC_BK;
+                    tma_load_2d(st, &mA_hi, kx, m0, full(s));
+                    tma_load_2d(st + TC_A_BYTES, &mA_lo, kx, m0, full(s));
+                    tma_load_2d(st + 2 * TC_A_BYTES, &mX_hi, kx, n0, full(s));
+                    tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &mX_lo, kx, n0, full(s));
                 }
-                if (*(volatile int *)&abort_flag) break;
-                const uint32_t st = base + s * TC_STAGE_BYTES;
-                mbar_expect_tx(full(s), TC_STAGE_BYTES);
-                const int kx = kb * TC_BK;
-                tma_load_2d(st, &mA_hi, kx, m0, full(s));
-                tma_load_2d(st + TC_A_BYTES, &mA_lo, kx, m0, full(s));
-                tma_load_2d(st + 2 * TC_A_BYTES, &mX_hi, kx, n0, full(s));
-                tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &mX_lo, kx, n0, full(s));
+            }
+            if (aborted()) {
+                // loads nobody consumed must land before the CTA's shared memory goes away
+                for (int j = (it > TC_STAGES ? it - TC_STAGES : 0); j < it; ++j)
+                    if (!mbar_wait(full(j % TC_STAGES), (j / TC_STAGES) & 1)) record_timeout(g.status);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = tf32_idesc(TC_BM, TC_BN);
-            bool ok = true;
-            for (int kb = 0; kb < nk && ok; ++kb) {
-                const int s = kb % TC_STAGES;
-                if (!mbar_wait(full(s), (kb / TC_STAGES) & 1)) {
-                    record_timeout(g.status);
-                    abort_flag = 1;
-                    ok = false;
+            int it = 0, i = 0;
+            for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x, ++i) {
+                const int a = i & 1;
+                if (i >= 2 && !mbar_wait(acc_empty(a), ((i >> 1) - 1) & 1)) {
+                    fail();
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-                const uint32_t st = base + s * TC_STAGE_BYTES;
+                const uint32_t d = tmem + (uint32_t)(a * TC_BN);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % TC_STAGES;
+                    if (!mbar_wait(full(s), (it / TC_STAGES) & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+                    const uint32_t st = base + s * TC_STAGE_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < TC_BK / 8; ++kk) {
-                    const uint64_t a_hi = sw128_desc(st + kk * 32);
-                    const uint64_t a_lo = sw128_desc(st + TC_A_BYTES + kk * 32);
-                    const uint64_t x_hi = sw128_desc(st + 2 * TC_A_BYTES + kk * 32);
-                    const uint64_t x_lo = sw128_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
-                    mma_tf32(tmem, a_hi, x_hi, idesc, (kb | kk) != 0);
-                    mma_tf32(tmem, a_hi, x_lo, idesc, 1);
-                    mma_tf32(tmem, a_lo, x_hi, idesc, 1);
+                    for (int kk = 0; kk < TC_BK / 8; ++kk) {
+                        const uint64_t a_hi = sw128_desc(st + kk * 32);
+                        const uint64_t a_lo = sw128_desc(st + TC_A_BYTES + kk * 32);
+                        const uint64_t x_hi = sw128_desc(st + 2 * TC_A_BYTES + kk * 32);
+                        const uint64_t x_lo = sw128_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
+                        mma_tf32(d, a_hi, x_hi, idesc, (kb | kk) != 0);
+                        mma_tf32(d, a_hi, x_lo, idesc, 1);
+                        mma_tf32(d, a_lo, x_hi, idesc, 1);
+                    }
+                    mma_commit(empty(s));  // the stage is free once these MMAs have read it
                 }
-                mma_commit(empty(s));  // the stage is free once these MMAs have read it
+                mma_commit(acc_full(a));  // accumulator a complete (or abandoned)
+                if (!ok) break;
             }
-            mma_commit(done_bar);  // accumulator complete (or abandoned)
+            // every MMA issued here has finished before tensor memory is released
+            mma_commit(drain);
+            if (!mbar_wait(drain, 0)) record_timeout(g.status);
         }
     } else {
         // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31.  A thread owns
-        // one row of the tile; C is read a 32-column chunk at a time into
+        // one row of a tile; C is read a 32-column chunk at a time into
         // registers (32 loads in flight), the next chunk's loads are issued
-        // before the current chunk is written, and the first chunk is
-        // fetched while the main loop still runs.
+        // before the current chunk is written, and a tile's first chunk is
+        // fetched while its accumulator is still being computed.
         const int quarter = warp & 3;
-        const int64_t gr = m0 + 32 * quarter + lane;
-        const bool row_ok = gr < g.M;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-        float cnext[32];
-        auto fetch = [&](int chunk, float (&dst)[32]) {
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
+            const int64_t gr = m0 + 32 * quarter + lane;
+            const bool row_ok = gr < g.M;
+            float cnext[32];
+            auto fetch = [&](int chunk, float(&dst)[32]) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int64_t gc = n0 + chunk * 32 + j;
-                dst[j] = (row_ok && gc < g.N) ? g.C[gc * g.ldc + gr] : 0.f;
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t gc = n0 + chunk * 32 + j;
+                    dst[j] = (row_ok && gc < g.N) ? g.C[gc * g.ldc + gr] : 0.f;
+                }
+            };
+            fetch(0, cnext);
+            if (!mbar_wait(acc_full(a), (i >> 1) & 1)) {
+                if (lane == 0) fail();
+                break;
             }
-        };
-        fetch(0, cnext);
-        const bool ok = mbar_wait(done_bar, 0);
-        if (!ok) {
-            if (lane == 0) record_timeout(g.status);
-        } else if (!*(volatile int *)&abort_flag) {
+            if (aborted()) break;
             asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * TC_BN);
 #pragma unroll 1
             for (int chunk = 0; chunk < TC_BN / 32; ++chunk) {
                 float ccur[32];
@@ -252,6 +302,12 @@ __global__ void __launch_bounds__(192, 1)
                       "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
                     : "r"(lane_addr + (uint32_t)(chunk * 32)));
                 asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                if (chunk + 1 == TC_BN / 32) {
+                    // every TMEM read of accumulator a is done: hand it back
+                    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty(a));
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
