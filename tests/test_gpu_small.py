@@ -160,3 +160,30 @@ def test_persistent_f32_path_many_items(env, m, n, batch):
     warps in flight."""
     L, B = ti.generate("f32", m, n, batch, kind="dd64", seed=m + n)
     _parity(env, "f32", L, B, 0.5, f"pipe m={m} n={n} batch={batch}")
+
+
+@pytest.mark.parametrize("m", [32, 48, 64])
+@pytest.mark.parametrize("geom", ["padded", "gaps", "shared_a"])
+def test_persistent_f32_strided_layouts(env, m, geom):
+    """Layouts the tensor-copy kernel must describe exactly (or hand to the
+    fallback): leading dimensions above m, gaps between systems, and one L
+    shared by every system (batch stride 0); the device status word stays
+    clear."""
+    n, batch = 64, 700
+    L, B = ti.generate("f32", m, n, batch, kind="dd64", seed=m)
+    kw = {}
+    if geom == "padded":
+        kw = dict(lda=m + 4, ldb=m + 8)
+    elif geom == "gaps":
+        kw = dict(stride_a=m * m + 64, stride_b=m * n + 32)
+    if geom == "shared_a":
+        L[:] = L[0]
+        a, b, geo = storage_pair(L[:1], B)
+        geo["batch"], geo["sa"] = batch, 0
+        b = ti.to_storage(B, "col")
+        raw = gpu_solve_buffers("f32", a, b, geo, 1.0, env["torch"], env["tg"])
+        ref = oracle_buffers("f32", a, b, geo, 1.0, env["oracle"])
+        assert_parity("f32", logical(raw, geo), logical(ref, geo), f"shared A m={m}")
+    else:
+        _parity(env, "f32", L, B, 1.0, f"{geom} m={m}", **kw)
+    assert env["tg"].trsm_device_status() == 0

@@ -1,6 +1,8 @@
 // Internal interfaces between the C ABI (api.cu) and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -77,7 +79,12 @@ inline size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int6
 bool tc_update_usable(int64_t M, int64_t N, int64_t K);
 int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
                   float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st);
-// Device status word of the bounded waits (synchronises the device).
+// Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).
+int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                   const uint32_t *box, bool swizzle128);
+// Device status word of the bounded waits: its device address (for the
+// kernels), and its value (synchronises the device).
+int device_status_word(int **out);
 int device_status(int clear);
 
 int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);

@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "small_kernels.cuh"
+#include "mbarrier.cuh"
 
 namespace trsm {
 
@@ -469,6 +470,213 @@ __global__ void __launch_bounds__(64 * kPipePairs, 1) small_pipe_f32_kernel(cons
     cp_async_wait_all();
 }
 
+// ---------------------------------------------------------------------------
+// Persistent f32 kernel on the TMA engine (m = 32, 48, 64).  Same work split
+// as the kernel above -- pairs of warps, a two-stage ring per pair, one
+// column per lane in registers -- but every HBM transfer is a tiled tensor
+// copy, off the load/store pipe that the L broadcasts keep busy:
+//   in   the lower 32 x 32 boxes of L (3 for m = 64) and the RHS slice as
+//        32-row x 64-column boxes, with the 128-byte shared-memory swizzle
+//        (16-byte chunk q of a 128-byte line c sits at chunk q ^ (c % 8)), so
+//        that a lane reading its own column meets no bank conflicts;
+//   out  X is written back over its RHS column and leaves as the same boxes
+//        (the tensor store clips columns past n and rows past m).
+// Per item that is a handful of copies, where per-column copies would be
+// limited by the copy engine's rate for small transfers.  Shapes the tensor
+// maps cannot describe take the kernel above.
+// ---------------------------------------------------------------------------
+template <int M>
+struct SwzStage {
+    static_assert(M == 32 || M == 48 || M == 64, "32-row boxes");
+    static constexpr int NR = (M + 31) / 32;                   // 32-row blocks
+    static constexpr int kLFloats = NR * (NR + 1) / 2 * 1024;  // lower boxes of L, 4 KB each
+    static constexpr int kBFloats = NR * 2048;                 // RHS boxes, 8 KB each
+    static constexpr int kElems = kLFloats + kBFloats;
+    static constexpr uint32_t kBytes = 4u * kElems;
+    // rows 4q .. 4q+3 of column k of L (box of row block q/8 and column block k/32)
+    static __host__ __device__ constexpr int loff(int k, int q) {
+        return ((q / 8) * (q / 8 + 1) / 2 + k / 32) * 1024 + (k % 32) * 32 + (((q % 8) ^ (k % 8)) * 4);
+    }
+    static __host__ __device__ constexpr int lel(int i, int k) { return loff(k, i / 4) + i % 4; }
+    // rows 4q .. 4q+3 of column c of the RHS slice
+    static __device__ __forceinline__ int boff(int c, int q) {
+        return kLFloats + (q / 8) * 2048 + c * 32 + (((q % 8) ^ (c & 7)) * 4);
+    }
+};
+
+// The substitution of RegDiag2 (two rows per step, CPT columns per lane) on
+// the swizzled image; 1/L_kk comes from lane k % 32 of dlo (k < 32) or dhi.
+template <int M, int KP, int CPT>
+struct SwzDiag2 {
+    static __device__ __forceinline__ void run(const float *__restrict__ st, float dlo, float dhi,
+                                               f32x2 (&bp)[CPT][M / 2]) {
+        using S = SwzStage<M>;
+        if constexpr (2 * KP < M) {
+            constexpr int k0 = 2 * KP, k1 = k0 + 1;
+            const float d0 = __shfl_sync(0xffffffffu, k0 < 32 ? dlo : dhi, k0 % 32);
+            const float d1 = __shfl_sync(0xffffffffu, k1 < 32 ? dlo : dhi, k1 % 32);
+            const float l10 = st[S::lel(k1, k0)];
+            f32x2 n0[CPT], n1[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float b0, b1;
+                unpack2(bp[c][KP], b0, b1);
+                const float x0 = b0 * d0;
+                const float x1 = fmaf(-l10, x0, b1) * d1;
+                bp[c][KP] = pack2(x0, x1);
+                n0[c] = pack2(-x0, -x0);
+                n1[c] = pack2(-x1, -x1);
+            }
+            constexpr int PF = KP + 1;
+            constexpr bool odd = (PF & 1) && PF < M / 2;
+            if constexpr (odd) {  // rows 2PF, 2PF+1: the upper half of chunk PF/2
+                const f32x2 l0 = *reinterpret_cast<const f32x2 *>(st + S::loff(k0, PF / 2) + 2);
+                const f32x2 l1 = *reinterpret_cast<const f32x2 *>(st + S::loff(k1, PF / 2) + 2);
+#pragma unroll
+                for (int c = 0; c < CPT; ++c) bp[c][PF] = ffma2(l1, n1[c], ffma2(l0, n0[c], bp[c][PF]));
+            }
+            constexpr int Q0 = (odd ? PF + 1 : PF) / 2, NQ = M / 4 - Q0;  // whole chunks left
+            constexpr int QB = CPT == 2 ? 4 : 8;                          // chunks per load batch
+#pragma unroll
+            for (int qb = 0; qb < NQ; qb += QB) {
+                ulonglong2 a[QB], b[QB];
+#pragma unroll
+                for (int u = 0; u < QB; ++u)
+                    if (qb + u < NQ) {
+                        a[u] = *reinterpret_cast<const ulonglong2 *>(st + S::loff(k0, Q0 + qb + u));
+                        b[u] = *reinterpret_cast<const ulonglong2 *>(st + S::loff(k1, Q0 + qb + u));
+                    }
+#pragma unroll
+                for (int u = 0; u < QB; ++u)
+                    if (qb + u < NQ) {
+                        const int p = 2 * (Q0 + qb + u);
+#pragma unroll
+                        for (int c = 0; c < CPT; ++c) {
+                            bp[c][p] = ffma2(b[u].x, n1[c], ffma2(a[u].x, n0[c], bp[c][p]));
+                            bp[c][p + 1] = ffma2(b[u].y, n1[c], ffma2(a[u].y, n0[c], bp[c][p + 1]));
+                        }
+                    }
+            }
+            SwzDiag2<M, KP + 1, CPT>::run(st, dlo, dhi, bp);
+        }
+    }
+};
+
+// WPI warps per item: 2 (a pair, one column per lane: 8 warps per SM) or 1
+// (two columns per lane, half the L broadcasts per item, 4 warps per SM);
+// units of WPI warps per CTA, as many as the stages fit.  Measured on GB300:
+// pairs are faster at m = 64, single warps at m = 32 and 48.
+template <int WPI>
+struct TmaUnits {
+    static constexpr int kUnits = WPI == 2 ? kPipePairs : 4;
+    static constexpr int kThreads = 32 * WPI * kUnits;
+};
+
+__device__ __forceinline__ void unit_sync(int unit, int nthreads) {
+    if (nthreads == 32) __syncwarp();
+    else asm volatile("bar.sync %0, %1;\n" ::"r"(unit + 1), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ bool unit_any(int unit, int nthreads, bool flag) {
+    if (nthreads == 32) return __any_sync(0xffffffffu, flag);
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "r"(unit + 1), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+template <int M, int WPI>
+__global__ void __launch_bounds__(TmaUnits<WPI>::kThreads, 1)
+    small_tma_f32_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                         const int n, const float alpha, const int64_t items, int *status) {
+    using S = SwzStage<M>;
+    constexpr int NR = S::NR, UNITS = TmaUnits<WPI>::kUnits, UT = 32 * WPI, CPT = 2 / WPI;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[UNITS][2];
+    const int tid = threadIdx.x;
+    const int unit = tid / UT, wu = (tid / 32) % WPI, lane = tid & 31;
+    const bool leader = (tid % UT) == 0;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;  // the swizzle pattern repeats every 1024 bytes
+    float *my = reinterpret_cast<float *>(smem_raw + (sbase - raw)) + unit * 2 * S::kElems;
+    if (tid < 2 * UNITS) mbar_init(smem_u32(&full_bar[tid >> 1][tid & 1]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncthreads();
+
+    const int slices = (n + 63) / 64;
+    auto issue = [&](int64_t item, int s) {  // the unit's leader
+        const int sys = (int)(item / slices);
+        const int j0 = (int)(item - (int64_t)sys * slices) * 64;
+        const uint32_t bar = smem_u32(&full_bar[unit][s]);
+        const uint32_t st = smem_u32(my + s * S::kElems);
+        mbar_expect_tx(bar, S::kBytes);
+        for (int rb = 0; rb < NR; ++rb)
+            for (int cb = 0; cb <= rb; ++cb)
+                tma_load_3d(st + 4u * (uint32_t)((rb * (rb + 1) / 2 + cb) * 1024), &mapA, 32 * rb, 32 * cb, sys, bar);
+        for (int rb = 0; rb < NR; ++rb)
+            tma_load_3d(st + 4u * (uint32_t)(S::kLFloats + rb * 2048), &mapB, 32 * rb, j0, sys, bar);
+    };
+
+    int64_t item = (int64_t)blockIdx.x * UNITS + unit;
+    const int64_t step = (int64_t)gridDim.x * UNITS;
+    if (leader && item < items) issue(item, 0);
+    for (int it = 0; item < items; ++it, item += step) {
+        const int s = it & 1;
+        const bool more = item + step < items;
+        if (leader && more) {
+            bulk_wait_read<0>();  // the last item's stores have read stage s^1
+            issue(item + step, s ^ 1);
+        }
+        const bool ok = mbar_wait(smem_u32(&full_bar[unit][s]), (uint32_t)(it >> 1) & 1u);
+        if (unit_any(unit, UT, !ok)) {
+            // a copy never completed: report, let the copies in flight land, stop
+            if (leader) record_timeout(status);
+            mbar_wait(smem_u32(&full_bar[unit][s]), (uint32_t)(it >> 1) & 1u);
+            if (more) mbar_wait(smem_u32(&full_bar[unit][s ^ 1]), (uint32_t)((it + 1) >> 1) & 1u);
+            break;
+        }
+        float *cur = my + s * S::kElems;
+        const float dlo = 1.0f / cur[S::lel(lane, lane)];
+        const float dhi = (M > 32 && lane + 32 < M) ? 1.0f / cur[S::lel(lane + 32, lane + 32)] : 0.f;
+        int col[CPT];  // columns of the slice
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) col[c] = 32 * (wu + c) + lane;
+        f32x2 bp[CPT][M / 2];
+        const f32x2 a2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int q = 0; q < M / 4; ++q) {
+                const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(cur + S::boff(col[c], q));
+                bp[c][2 * q] = ffma2(a2, v.x, 0ull);
+                bp[c][2 * q + 1] = ffma2(a2, v.y, 0ull);
+            }
+        SwzDiag2<M, 0, CPT>::run(cur, dlo, dhi, bp);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int q = 0; q < M / 4; ++q)
+                *reinterpret_cast<ulonglong2 *>(cur + S::boff(col[c], q)) =
+                    make_ulonglong2(bp[c][2 * q], bp[c][2 * q + 1]);
+        fence_proxy_async_smem();
+        unit_sync(unit, UT);
+        if (leader) {
+            const int sys = (int)(item / slices);
+            const int j0 = (int)(item - (int64_t)sys * slices) * 64;
+            for (int rb = 0; rb < NR; ++rb)
+                tma_store_3d(&mapB, 32 * rb, j0, sys, smem_u32(cur + S::kLFloats + rb * 2048));
+            bulk_commit();
+        }
+    }
+    if (leader) bulk_wait<0>();  // every store complete before the CTA's shared memory goes away
+}
+
 // CTA: SPC systems x (W / CPT) threads each.  Thread g of a system owns
 // columns g + c*(W/CPT), c < CPT, of the CTA's column slice.
 template <typename T, int M, int W, int CPT, int RC, int SPC>
@@ -594,15 +802,60 @@ static int launch_pipe_f32(const SmallGeom &g, float alpha, cudaStream_t st) {
     return launch_status();
 }
 
+// The TMA kernel when the tensor maps accept the strides (base, leading
+// dimensions and batch strides 16-byte multiples, batch < 2^31);
+// kFastNotApplicable otherwise.
+constexpr int kTmaNotApplicable = -100001;
+
+template <int M, int WPI>
+static int launch_tma_f32(const SmallGeom &g, float alpha, cudaStream_t st) {
+    using S = SwzStage<M>;
+    if (g.batch >= (int64_t(1) << 31)) return kTmaNotApplicable;
+    CUtensorMap ma, mb;
+    const uint64_t da[3] = {(uint64_t)M, (uint64_t)M, (uint64_t)g.batch};
+    const uint64_t sa[2] = {(uint64_t)g.lda * 4, (uint64_t)g.sA * 4};
+    const uint32_t ba[3] = {32, 32, 1};
+    if (encode_f32_map(&ma, g.A, 3, da, sa, ba, true)) return kTmaNotApplicable;
+    const uint64_t db[3] = {(uint64_t)M, (uint64_t)g.n, (uint64_t)g.batch};
+    const uint64_t sb[2] = {(uint64_t)g.ldb * 4, (uint64_t)g.sB * 4};
+    const uint32_t bb[3] = {32, 64, 1};
+    if (encode_f32_map(&mb, g.B, 3, db, sb, bb, true)) return kTmaNotApplicable;
+    constexpr int UNITS = TmaUnits<WPI>::kUnits;
+    constexpr size_t smem = (size_t)UNITS * 2 * S::kElems * sizeof(float) + 1024;
+    static_assert(smem <= 227 * 1024, "TMA kernel shared memory");
+    auto kern = small_tma_f32_kernel<M, WPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    int *status = nullptr;
+    const int rc = device_status_word(&status);
+    if (rc) return rc;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 152;
+    const int64_t items = g.batch * ((g.n + 63) / 64);
+    int64_t ctas = (items + UNITS - 1) / UNITS;
+    if (ctas > sms) ctas = sms;  // persistent: one CTA per SM
+    kern<<<(unsigned)ctas, TmaUnits<WPI>::kThreads, smem, st>>>(ma, mb, g.n, alpha, items, status);
+    return launch_status();
+}
+
 template <typename T, int M>
 static int launch_fast_m(const SmallGeom &g, T alpha, cudaStream_t st) {
     if constexpr (std::is_same<T, float>::value) {
-        if (g.n <= 32) return launch_reg_f32<M, 32>(g, alpha, st);
+        if (g.n <= 16) return launch_reg_f32<M, 32>(g, alpha, st);
         if constexpr (M >= 16) {
-            // many items: the persistent pipelined kernel; a handful: one CTA
-            // per 4 systems finishes sooner
-            if (g.batch * ((g.n + 63) / 64) >= 4 * 152) return launch_pipe_f32<M>(g, alpha, st);
+            // many items: a persistent kernel; a handful: one CTA per few
+            // systems finishes sooner
+            if (g.batch * ((g.n + 63) / 64) >= 4 * 152) {
+                if constexpr (M % 16 == 0 && M >= 32) {
+                    const int rc = launch_tma_f32<M, (M == 64 ? 2 : 1)>(g, alpha, st);
+                    if (rc != kTmaNotApplicable) return rc;
+                }
+                return launch_pipe_f32<M>(g, alpha, st);
+            }
         }
+        if (g.n <= 32) return launch_reg_f32<M, 32>(g, alpha, st);
         return launch_reg_f32<M, 64>(g, alpha, st);
     }
     constexpr int CPT = std::is_same<T, float>::value ? 2 : 1;

@@ -21,22 +21,6 @@ std::mutex g_mu;
 int *g_status_ptr[kMaxDev] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int status_word(int **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (dev < 0 || dev >= kMaxDev) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_status_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_device_status);
-        if (e != cudaSuccess) return cuda_status(e);
-        g_status_ptr[dev] = static_cast<int *>(p);
-    }
-    *out = g_status_ptr[dev];
-    return TRSM_SUCCESS;
-}
-
 int encoder(PFN_cuTensorMapEncodeTiled_v12000 *out) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_encode) {
@@ -75,6 +59,47 @@ int split(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, float 
 
 }  // namespace
 
+// Device address of the status word for the current device (looked up once).
+int device_status_word(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDev) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return TRSM_SUCCESS;
+}
+
+// Tiled tensor map of an f32 tensor (rank <= 5, dims innermost first,
+// strides in bytes for dims 1..rank-1), optionally with the 128-byte
+// shared-memory swizzle.  Out-of-range elements load as zero.
+int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                   const uint32_t *box, bool swizzle128) {
+    if (rank < 1 || rank > 5) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    const int rc = encoder(&enc);
+    if (rc) return rc;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, e,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TRSM_SUCCESS : TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
+}
+
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb) {
     return (size_t)(2 * round256(m * nb * 4) + 2 * round256(n * nb * 4));
 }
@@ -102,7 +127,7 @@ int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
     if ((rc = make_map(&mx_hi, x_hi, N, K, K, TC_BN))) return rc;
     if ((rc = make_map(&mx_lo, x_lo, N, K, K, TC_BN))) return rc;
     int *status = nullptr;
-    if ((rc = status_word(&status))) return rc;
+    if ((rc = device_status_word(&status))) return rc;
     TcArgs g;
     g.M = M;
     g.N = N;
@@ -129,7 +154,7 @@ int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
 
 int device_status(int clear) {
     int *p = nullptr;
-    int rc = status_word(&p);
+    int rc = device_status_word(&p);
     if (rc) return rc;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e);

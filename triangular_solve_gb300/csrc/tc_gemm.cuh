@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "mbarrier.cuh"
 
 namespace trsm {
 
@@ -41,7 +42,6 @@ constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 32 KB
 constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 96 KB
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column FP32 accumulators
 constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
-constexpr uint32_t TC_WAIT_LIMIT = 1u << 24;  // try_wait rounds before giving up
 
 struct TcArgs {
     int64_t M, N, K;
@@ -50,34 +50,6 @@ struct TcArgs {
     float beta;
     int *status;  // device status word (0 = ok)
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Bounded wait for the phase with the given parity; false when it expired.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < TC_WAIT_LIMIT; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
     asm volatile(
@@ -123,13 +95,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void record_timeout(int *status) {
-    if (status) atomicExch(status, TRSM_ERR_DEVICE_TIMEOUT);
-}
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
 
 // Persistent: one CTA per SM walks the output tiles t = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  (consecutive CTAs take consecutive row tiles of
