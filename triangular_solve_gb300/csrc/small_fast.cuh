@@ -96,7 +96,9 @@ struct FastChunks {
 #pragma unroll
                     for (int u = 0; u < V; ++u) b[c][g0 + u] = mul(alpha, v[u]);
                 }
-#pragma unroll
+            // rows solved by earlier chunks: a rolled loop (unrolled by 4),
+            // so the code stays small enough for the instruction cache
+#pragma unroll 4
             for (int k = 0; k < CH * RC; ++k) {
                 T x[CPT];
 #pragma unroll
@@ -859,7 +861,11 @@ static int launch_fast_m(const SmallGeom &g, T alpha, cudaStream_t st) {
         return launch_reg_f32<M, 64>(g, alpha, st);
     }
     constexpr int CPT = std::is_same<T, float>::value ? 2 : 1;
-    constexpr int RC = (sizeof(T) >= 16 && M > 32) ? (M % 32 == 0 ? 32 : M / 2) : M;
+    // row chunk: 16 rows for the complex types, 32 for f64; only the chunk's
+    // own triangle is unrolled (a whole unrolled 64-row triangle of c64
+    // outgrows the instruction cache: "no instruction" stalls dominated)
+    constexpr int RCX = Elem<T>::kComplex ? 16 : 32;
+    constexpr int RC = (M > RCX && M % RCX == 0) ? RCX : M;
     if (g.n <= 32) return launch_fast_mw<T, M, 32, CPT, RC>(g, alpha, st);
     return launch_fast_mw<T, M, 64, CPT, RC>(g, alpha, st);
 }
