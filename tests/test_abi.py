@@ -51,9 +51,10 @@ def test_workspace_bytes(lib):
     w = 8 * 128 * 128 * 4
     x = 128 * 72 * 4
     r = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    # f32 also holds the TF32 head/tail copies of the L panel (m x NB) and of
-    # the X panel (n x NB) for the tensor-core update
-    tc = 2 * r(1000 * 128 * 4) + 2 * r(70 * 128 * 4)
+    # f32 also holds the TF32 head/tail copies of the tensor-core operands:
+    # the A panel (m x NB), the X panel (n x NB) and the split X_t the apply
+    # leaves for the update (n x NB)
+    tc = 2 * r(1000 * 128 * 4) + 4 * r(70 * 128 * 4)
     assert tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 128) == r(w) + 2 * r(x) + tc
     assert tg.trsm_llnn_workspace_bytes("c128", 1000, 70, 512) == r(2 * 512 * 512 * 16) + 2 * r(512 * 72 * 16)
     with pytest.raises(ValueError):

@@ -136,13 +136,17 @@ def test_large_fp32_workload(env, dtype):
     assert_parity(dtype, xg, xr, f"{dtype} m={m}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
 @pytest.mark.parametrize("nb", [128, 256, 512])
 @pytest.mark.parametrize("m,n", [(1000, 777), (1500, 300), (2100, 1030)])
-def test_tensor_core_update_f32_ragged(env, nb, m, n):
-    """f32 shapes that take the tcgen05 (3xTF32) trailing update: ragged
-    row and column tiles, every block size; the device status word stays
-    clear (no bounded wait expired)."""
-    L, B = ti.generate("f32", m, n, 1, kind="ddm", seed=m + 3 * n)
-    xg, xr = _ex_solve(env, "f32", L, B, -0.5, nb, lda=m + 4, ldb=m + 8)
+def test_tensor_core_products_ragged(env, dtype, nb, m, n):
+    """Shapes that take the tcgen05 (3xTF32) products -- the f32 apply and
+    update, the c64 update in real form with a complex beta at t = 0 --:
+    ragged row and column tiles, every block size, blocks that fall back to
+    the FMA-pipe kernels; the device status word stays clear (no bounded
+    wait expired)."""
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + 3 * n)
+    alpha = (-0.5 + 0.75j) if ti.IS_COMPLEX[dtype] else -0.5
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, nb, lda=m + 4, ldb=m + 8)
     assert env["tg"].trsm_device_status() == 0
-    assert_parity("f32", xg, xr, f"tc f32 m={m} n={n} nb={nb}")
+    assert_parity(dtype, xg, xr, f"tc {dtype} m={m} n={n} nb={nb}")

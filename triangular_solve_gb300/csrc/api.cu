@@ -130,7 +130,7 @@ int solve(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const 
 
     const int eb = elem_bytes(dtype);
     if (nb == 0) nb = nearest_nb(dtype, m);
-    const size_t need = blocked_workspace_bytes(eb, m, n, nb);
+    const size_t need = blocked_workspace_bytes((int)dtype, m, n, nb);
     // Row-major systems run through the column-major path on transposed
     // copies held after the workspace.
     const int64_t tl_bytes = layout == TRSM_ROW_MAJOR ? ((m * m * eb + 255) / 256) * 256 : 0;
@@ -258,7 +258,7 @@ size_t trsm_llnn_workspace_bytes(trsm_dtype_t dtype, int64_t m, int64_t n, int64
     if (nb != 0 && nb != 128 && nb != 256 && nb != 512) return (size_t)-1;
     if (m <= 64 || n == 0) return 0;
     if (nb == 0) nb = nearest_nb(dtype, m);
-    return blocked_workspace_bytes(eb, m, n, nb);
+    return blocked_workspace_bytes((int)dtype, m, n, nb);
 }
 
 static int ex_common(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda,
@@ -280,7 +280,7 @@ static int ex_common(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha
     if (!B || !aligned(B, eb)) return -7;
     if (m <= 64 && n > 64LL * 65535) return -3;
     if (m > 64 && !zero) {
-        const size_t need = blocked_workspace_bytes(eb, m, n, nb ? nb : nearest_nb(dtype, m));
+        const size_t need = blocked_workspace_bytes((int)dtype, m, n, nb ? nb : nearest_nb(dtype, m));
         if (!workspace || !aligned(workspace, 256) || ws_bytes < need) return TRSM_ERR_WORKSPACE;
     }
     return solve(dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, nb, workspace, ws_bytes, false,

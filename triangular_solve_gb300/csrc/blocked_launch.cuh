@@ -71,6 +71,10 @@ static int update_launch(int64_t M, int64_t N, int64_t K, const T *A, int64_t ld
         if (tc_panels && tc_update_usable(M, N, K))
             return tc_update_f32(M, N, K, A, lda, X, ldx, C, ldc, beta, Mmax, tc_panels, st);
     }
+    if constexpr (std::is_same<T, float2>::value) {
+        if (tc_panels && tc_update_usable(M, 2 * N, 2 * K))
+            return tc_update_c64(M, N, K, A, lda, X, ldx, C, ldc, beta, Mmax, tc_panels, st);
+    }
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
         const bool aligned = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
                              ((lda * (int64_t)sizeof(T)) % 16 == 0);
@@ -194,7 +198,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + round256(tbk * nb * nb * (int64_t)sizeof(T)));
     T *Pw = reinterpret_cast<T *>(reinterpret_cast<char *>(Xw) + round256(nb * ldx * (int64_t)sizeof(T)));
     void *tc_panels = nullptr;
-    if constexpr (std::is_same<T, float>::value)
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value)
         tc_panels = reinterpret_cast<char *>(Pw) + round256(nb * ldx * (int64_t)sizeof(T));
 
     PhaseTimer timer;
@@ -224,6 +228,26 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         // Phase 1: X_t = gamma * D_t^{-1} R_t into the panel (gamma = alpha at
         // t = 0; later block rows already carry alpha through the updates).
         const T gamma = (t == 0) ? alpha : one;
+        if constexpr (std::is_same<T, float>::value) {
+            // both products on the tensor cores: X_t straight over R_t in B,
+            // its split copy straight into the update's operand panels
+            const bool has_update = r0 + nb < m;
+            if (tc_panels && tc_apply_usable(mb, n) &&
+                (!has_update || tc_update_usable(m - r0 - nb, n, nb))) {
+                timer.begin();
+                rc = tc_apply_f32(mb, n, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
+                if (rc || (rc = timer.end(1))) return rc;
+                timer.begin();
+                if (has_update) {
+                    const T beta = (t == 0) ? alpha : one;
+                    rc = tc_update_f32(m - r0 - nb, n, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
+                                       a.ldb, beta, m, tc_panels, st);
+                    if (rc) return rc;
+                }
+                if ((rc = timer.end(2))) return rc;
+                continue;
+            }
+        }
         timer.begin();
         rc = kSpNotApplicable;
         if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {

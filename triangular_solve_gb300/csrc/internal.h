@@ -65,20 +65,33 @@ struct BlockedArgs {
 // rounded up to 256 bytes.
 inline int64_t panel_ld(int64_t n) { return ((n > 0 ? n : 1) + 3) / 4 * 4; }
 inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
-// f32 adds the TF32 head/tail panels of the tensor-core update
-// (tc_panel_bytes: L panel and X_t panel, two copies each, K-major).
+// f32 adds the TF32 head/tail panels of the tensor-core products
+// (tc_panel_bytes: the A operand -- L panel or D_t^-1 --, the X operand and
+// the split X_t the apply leaves for the update, two copies each, K-major).
+// c64 adds the real-form operands of its tensor-core update
+// (tc_panel_bytes_c64: A' = m x 2nb, X' = 2n x 2nb, two copies each).
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb);
-inline size_t blocked_workspace_bytes(int elem_bytes, int64_t m, int64_t n, int64_t nb) {
+size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb);
+inline size_t blocked_workspace_bytes(int dtype, int64_t m, int64_t n, int64_t nb) {
+    const int elem_bytes = dtype == 0 ? 4 : dtype == 3 ? 16 : 8;
     const int64_t tb = (m + nb - 1) / nb;
     size_t b = (size_t)(round256(tb * nb * nb * elem_bytes) + 2 * round256(nb * panel_ld(n) * elem_bytes));
-    if (elem_bytes == 4) b += tc_panel_bytes(m, n, nb);
+    if (dtype == 0) b += tc_panel_bytes(m, n, nb);
+    if (dtype == 2) b += tc_panel_bytes_c64(m, n, nb);
     return b;
 }
 
-// Tensor-core (tcgen05, 3xTF32) f32 trailing update; see tc_gemm.cuh.
+// Tensor-core (tcgen05, 3xTF32) f32 products of the blocked path; see
+// tc_gemm.cuh / tc_gemm.cu.  tc_update_f32 with X == nullptr takes the split
+// X_t that tc_apply_f32(..., emit_split = true) left in the panels.
 bool tc_update_usable(int64_t M, int64_t N, int64_t K);
+bool tc_apply_usable(int64_t mb, int64_t N);
 int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
                   float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st);
+int tc_update_c64(int64_t M, int64_t N, int64_t K, const float2 *A, int64_t lda, const float2 *X, int64_t ldx,
+                  float2 *C, int64_t ldc, float2 beta, int64_t Mmax, void *panels, cudaStream_t st);
+int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, int64_t ldb, float gamma,
+                 int64_t Mmax, void *panels, bool emit_split, cudaStream_t st);
 // Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).
 int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
                    const uint32_t *box, bool swizzle128);

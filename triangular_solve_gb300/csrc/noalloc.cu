@@ -126,7 +126,7 @@ extern "C" int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const
     }
 
     const int nb = trsm_llnn_select_nb(dtype, m, n);  // the table's block size, as trsm_llnn uses
-    const size_t need = blocked_workspace_bytes(eb, m, n, nb);
+    const size_t need = blocked_workspace_bytes((int)dtype, m, n, nb);
     if (need > (size_t)TRSM_NOALLOC_SCRATCH_BYTES) return TRSM_ERR_WORKSPACE;
     void *scratch = nullptr;
     const int rc = scratch_on_current_device(&scratch);

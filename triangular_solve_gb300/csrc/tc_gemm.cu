@@ -100,8 +100,29 @@ int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t 
     return r == CUDA_SUCCESS ? TRSM_SUCCESS : TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
 }
 
+// Workspace of the tensor-core products, 256-byte aligned regions:
+//   a_hi, a_lo    the A operand (L panel, m x nb; or D_t^-1), K-major
+//   x_hi, x_lo    the X operand (n x nb), K-major
+//   xs_hi, xs_lo  X_t as split by the apply's epilogue for the next update
+struct TcPanels {
+    float *a_hi, *a_lo, *x_hi, *x_lo, *xs_hi, *xs_lo;
+};
+
+static TcPanels tc_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
+    TcPanels p;
+    char *c = static_cast<char *>(panels);
+    const size_t A = round256(m * nb * 4), X = round256(n * nb * 4);
+    p.a_hi = reinterpret_cast<float *>(c);
+    p.a_lo = reinterpret_cast<float *>(c + A);
+    p.x_hi = reinterpret_cast<float *>(c + 2 * A);
+    p.x_lo = reinterpret_cast<float *>(c + 2 * A + X);
+    p.xs_hi = reinterpret_cast<float *>(c + 2 * A + 2 * X);
+    p.xs_lo = reinterpret_cast<float *>(c + 2 * A + 3 * X);
+    return p;
+}
+
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb) {
-    return (size_t)(2 * round256(m * nb * 4) + 2 * round256(n * nb * 4));
+    return (size_t)(2 * round256(m * nb * 4) + 4 * round256(n * nb * 4));
 }
 
 bool tc_update_usable(int64_t M, int64_t N, int64_t K) {
@@ -109,33 +130,30 @@ bool tc_update_usable(int64_t M, int64_t N, int64_t K) {
     return M >= TC_BM && N >= TC_BN && K >= TC_BK && K % TC_BK == 0;
 }
 
-// C (M x N, column-major ldc) = beta*C - L_panel (M x K, column-major lda) *
-// X (K x N, row-major ldx), through TF32 head/tail panels in `panels`
-// (tc_panel_bytes(Mmax, N, K) bytes, 256-byte aligned).
-int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
-                  float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st) {
-    float *a_hi = static_cast<float *>(panels);
-    float *a_lo = reinterpret_cast<float *>(reinterpret_cast<char *>(a_hi) + round256(Mmax * K * 4));
-    float *x_hi = reinterpret_cast<float *>(reinterpret_cast<char *>(a_lo) + round256(Mmax * K * 4));
-    float *x_lo = reinterpret_cast<float *>(reinterpret_cast<char *>(x_hi) + round256(N * K * 4));
-    int rc = split(A, lda, M, K, a_hi, a_lo, K, st);         // L panel rows, K-major
-    if (!rc) rc = split(X, ldx, N, K, x_hi, x_lo, K, st);    // X_t columns, K-major
-    if (rc) return rc;
+bool tc_apply_usable(int64_t mb, int64_t N) {
+    // enough output tiles to occupy the GPU; with fewer the FMA-pipe apply,
+    // which has smaller tiles, finishes first (measured on GB300)
+    const int64_t tiles = ((mb + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN);
+    return tc_update_usable(mb, N, mb) && tiles >= 48;
+}
+
+namespace {
+
+int split_rows(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, float *lo, int64_t ldd,
+               cudaStream_t st) {
+    const dim3 grid((unsigned)((Kc + 127) / 128), (unsigned)(R < 65535 ? R : 65535));
+    split_rows_tf32_kernel<<<grid, 128, 0, st>>>(src, ks, R, Kc, hi, lo, ldd);
+    return launch_status();
+}
+
+int launch_tc(const float *a_hi, const float *a_lo, const float *x_hi, const float *x_lo, TcArgs g, cudaStream_t st) {
     CUtensorMap ma_hi, ma_lo, mx_hi, mx_lo;
-    if ((rc = make_map(&ma_hi, a_hi, M, K, K, TC_BM))) return rc;
-    if ((rc = make_map(&ma_lo, a_lo, M, K, K, TC_BM))) return rc;
-    if ((rc = make_map(&mx_hi, x_hi, N, K, K, TC_BN))) return rc;
-    if ((rc = make_map(&mx_lo, x_lo, N, K, K, TC_BN))) return rc;
-    int *status = nullptr;
-    if ((rc = device_status_word(&status))) return rc;
-    TcArgs g;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.C = C;
-    g.ldc = ldc;
-    g.beta = beta;
-    g.status = status;
+    int rc;
+    if ((rc = make_map(&ma_hi, a_hi, g.M, g.K, g.K, TC_BM))) return rc;
+    if ((rc = make_map(&ma_lo, a_lo, g.M, g.K, g.K, TC_BM))) return rc;
+    if ((rc = make_map(&mx_hi, x_hi, g.N, g.K, g.K, TC_BN))) return rc;
+    if ((rc = make_map(&mx_lo, x_lo, g.N, g.K, g.K, TC_BN))) return rc;
+    if ((rc = device_status_word(&g.status))) return rc;
     const cudaError_t e =
         cudaFuncSetAttribute(tc_update_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return cuda_status(e);
@@ -146,10 +164,101 @@ int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
     }
-    const int64_t tiles = ((M + TC_BM - 1) / TC_BM) * ((N + TC_BN - 1) / TC_BN);
+    const int64_t tiles = ((g.M + TC_BM - 1) / TC_BM) * ((g.N + TC_BN - 1) / TC_BN);
     const unsigned ctas = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
     tc_update_f32_kernel<<<ctas, 192, TC_SMEM, st>>>(ma_hi, ma_lo, mx_hi, mx_lo, g);
     return launch_status();
+}
+
+TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
+    TcArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.C = C;
+    g.ldc = ldc;
+    g.beta = 0.f;
+    g.beta_im = 0.f;
+    g.gamma = -1.f;
+    g.beta_zero = 0;
+    g.a_lower = 0;
+    g.cplx = 0;
+    g.xhi = g.xlo = nullptr;
+    g.ldxs = 0;
+    g.status = nullptr;
+    return g;
+}
+
+}  // namespace
+
+// C (M x N, column-major ldc) = beta*C - L_panel (M x K, column-major lda) *
+// X (K x N), through the TF32 head/tail panels in `panels` (tc_panel_bytes(
+// Mmax, N, K) bytes, 256-byte aligned).  X is either the row-major panel X
+// (ldx), split here, or -- X == nullptr -- the split copy that tc_apply_f32
+// left in the panels.
+int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
+                  float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st) {
+    const TcPanels p = tc_layout(panels, Mmax, N, K);
+    int rc = split(A, lda, M, K, p.a_hi, p.a_lo, K, st);  // L panel rows, K-major
+    if (rc) return rc;
+    const float *xh = p.xs_hi, *xl = p.xs_lo;
+    if (X) {
+        if ((rc = split(X, ldx, N, K, p.x_hi, p.x_lo, K, st))) return rc;  // X_t columns, K-major
+        xh = p.x_hi;
+        xl = p.x_lo;
+    }
+    TcArgs g = tc_args(M, N, K, C, ldc);
+    g.beta = beta;
+    return launch_tc(p.a_hi, p.a_lo, xh, xl, g, st);
+}
+
+// c64 trailing update C = beta*C - A X (A column-major lda, X the row-major
+// panel, ldx, all complex) as one real product of M x 2N x 2K on the
+// tensor cores (see split_c64_*).  Panels: tc_panel_bytes_c64(Mmax, N, K).
+int tc_update_c64(int64_t M, int64_t N, int64_t K, const float2 *A, int64_t lda, const float2 *X, int64_t ldx,
+                  float2 *C, int64_t ldc, float2 beta, int64_t Mmax, void *panels, cudaStream_t st) {
+    char *c = static_cast<char *>(panels);
+    const size_t Ab = round256(Mmax * 2 * K * 4), Xb = round256(2 * N * 2 * K * 4);
+    float *a_hi = reinterpret_cast<float *>(c), *a_lo = reinterpret_cast<float *>(c + Ab);
+    float *x_hi = reinterpret_cast<float *>(c + 2 * Ab), *x_lo = reinterpret_cast<float *>(c + 2 * Ab + Xb);
+    split_c64_a_kernel<<<dim3((unsigned)((M + 31) / 32), (unsigned)((K + 31) / 32)), dim3(32, 8), 0, st>>>(
+        A, lda, M, K, a_hi, a_lo);
+    int rc = launch_status();
+    if (rc) return rc;
+    split_c64_x_kernel<<<dim3((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32)), dim3(32, 8), 0, st>>>(
+        X, ldx, K, N, x_hi, x_lo);
+    if ((rc = launch_status())) return rc;
+    TcArgs g = tc_args(M, 2 * N, 2 * K, reinterpret_cast<float *>(C), 2 * ldc);
+    g.beta = beta.x;
+    g.beta_im = beta.y;
+    g.cplx = 1;
+    return launch_tc(a_hi, a_lo, x_hi, x_lo, g, st);
+}
+
+size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb) {
+    return (size_t)(2 * round256(m * 2 * nb * 4) + 2 * round256(2 * n * 2 * nb * 4));
+}
+
+// Block apply on the tensor cores: X_t = gamma * D_t^-1 R_t, written over
+// R_t (its block row of B: mb x N, column-major ldb); D_t^-1 is the
+// column-major lower-triangular block Wt (ld nb).  With emit_split the
+// epilogue also leaves X_t split, K-major, for tc_update_f32 (X == nullptr).
+int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, int64_t ldb, float gamma,
+                 int64_t Mmax, void *panels, bool emit_split, cudaStream_t st) {
+    const TcPanels p = tc_layout(panels, Mmax, N, nb);
+    int rc = split(Wt, nb, mb, mb, p.a_hi, p.a_lo, mb, st);  // rows of D_t^-1, K-major
+    if (!rc) rc = split_rows(Bt, ldb, N, mb, p.x_hi, p.x_lo, mb, st);  // columns of R_t
+    if (rc) return rc;
+    TcArgs g = tc_args(mb, N, mb, Bt, ldb);
+    g.beta_zero = 1;
+    g.gamma = gamma;
+    g.a_lower = 1;
+    if (emit_split) {
+        g.xhi = p.xs_hi;
+        g.xlo = p.xs_lo;
+        g.ldxs = nb;
+    }
+    return launch_tc(p.a_hi, p.a_lo, p.x_hi, p.x_lo, g, st);
 }
 
 int device_status(int clear) {

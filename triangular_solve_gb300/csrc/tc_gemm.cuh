@@ -43,11 +43,21 @@ constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 96 KB
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column FP32 accumulators
 constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
 
+// out = beta*C + gamma*(A X) (beta_zero: out = gamma*(A X), C not read),
+// stored to C; with xhi set, out is also stored split (TF32 head/tail) and
+// K-major, xhi[col * ldxs + row], as the X operand of a later product.
+// a_lower: A is lower triangular, so a row tile stops its K loop at its last
+// row.  cplx: the product is the real form of a complex one, output columns
+// 2j and 2j+1 being the real and imaginary parts of complex column j of C
+// (interleaved, ldc counted in floats), and beta = beta + i*beta_im.
 struct TcArgs {
     int64_t M, N, K;
     float *C;
     int64_t ldc;
-    float beta;
+    float beta, beta_im, gamma;
+    int beta_zero, a_lower, cplx;
+    float *xhi, *xlo;
+    int64_t ldxs;
     int *status;  // device status word (0 = ok)
 };
 
@@ -96,6 +106,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 
+
+// Round to TF32, nearest (ties away from zero).
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
 
 // Persistent: one CTA per SM walks the output tiles t = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  (consecutive CTAs take consecutive row tiles of
@@ -159,7 +176,8 @@ __global__ void __launch_bounds__(192, 1)
             int it = 0;
             for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
                 const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int nkt = g.a_lower ? min(nk, (m0 + TC_BM) / TC_BK) : nk;
+                for (int kb = 0; kb < nkt; ++kb, ++it) {
                     const int s = it % TC_STAGES;
                     if (it >= TC_STAGES && !mbar_wait(empty(s), ((it / TC_STAGES) - 1) & 1)) {
                         fail();
@@ -192,8 +210,10 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(a * TC_BN);
+                const int m0 = (t % tiles_m) * TC_BM;
+                const int nkt = g.a_lower ? min(nk, (m0 + TC_BM) / TC_BK) : nk;
                 bool ok = true;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                for (int kb = 0; kb < nkt; ++kb, ++it) {
                     const int s = it % TC_STAGES;
                     if (!mbar_wait(full(s), (it / TC_STAGES) & 1)) {
                         fail();
@@ -235,11 +255,15 @@ __global__ void __launch_bounds__(192, 1)
             const int64_t gr = m0 + 32 * quarter + lane;
             const bool row_ok = gr < g.M;
             float cnext[32];
+            // element (gr, gc) of C
+            auto coff = [&](int64_t gc) -> int64_t {
+                return g.cplx ? (gc >> 1) * g.ldc + 2 * gr + (gc & 1) : gc * g.ldc + gr;
+            };
             auto fetch = [&](int chunk, float(&dst)[32]) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int64_t gc = n0 + chunk * 32 + j;
-                    dst[j] = (row_ok && gc < g.N) ? g.C[gc * g.ldc + gr] : 0.f;
+                    dst[j] = (!g.beta_zero && row_ok && gc < g.N) ? g.C[coff(gc)] : 0.f;
                 }
             };
             fetch(0, cnext);
@@ -274,11 +298,31 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acc_empty(a));
                 }
-                if (row_ok) {
+                if (row_ok && g.cplx) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const int64_t gc = n0 + chunk * 32 + j;  // even: a (re, im) pair
+                        if (gc < g.N) {
+                            const float cr = ccur[j], ci = ccur[j + 1];
+                            const float ar = g.gamma * __uint_as_float(v[j]), ai = g.gamma * __uint_as_float(v[j + 1]);
+                            const float orr = fmaf(g.beta, cr, fmaf(-g.beta_im, ci, ar));
+                            const float oi = fmaf(g.beta, ci, fmaf(g.beta_im, cr, ai));
+                            *reinterpret_cast<float2 *>(g.C + coff(gc)) = make_float2(orr, oi);
+                        }
+                    }
+                } else if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int64_t gc = n0 + chunk * 32 + j;
-                        if (gc < g.N) g.C[gc * g.ldc + gr] = fmaf(g.beta, ccur[j], -__uint_as_float(v[j]));
+                        if (gc < g.N) {
+                            const float o = fmaf(g.beta, ccur[j], g.gamma * __uint_as_float(v[j]));
+                            g.C[gc * g.ldc + gr] = o;
+                            if (g.xhi) {
+                                const float h = to_tf32(o);
+                                g.xhi[gc * g.ldxs + gr] = h;
+                                g.xlo[gc * g.ldxs + gr] = to_tf32(o - h);
+                            }
+                        }
                     }
                 }
             }
@@ -297,11 +341,6 @@ __global__ void __launch_bounds__(192, 1)
 //   hi[r * ldd + k] = tf32(src[r + k * ks]),  lo = tf32(src - hi)
 // for r < R, k < Kc.  32 x 32 tiles through shared memory (src is read
 // along r, dst written along k).
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
 
 __global__ void split_tf32_kernel(const float *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
                                   float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
@@ -319,6 +358,77 @@ __global__ void split_tf32_kernel(const float *__restrict__ src, int64_t ks, int
             const float h = to_tf32(a);
             hi[r * ldd + k] = h;
             lo[r * ldd + k] = to_tf32(a - h);
+        }
+    }
+}
+
+// The same split for a source that is K-major already:
+//   hi[r * ldd + k] = tf32(src[r * ks + k]),  lo = tf32(src - hi).
+__global__ void split_rows_tf32_kernel(const float *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
+                                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= Kc) return;
+    for (int64_t r = blockIdx.y; r < R; r += gridDim.y) {
+        const float a = src[r * ks + k];
+        const float h = to_tf32(a);
+        hi[r * ldd + k] = h;
+        lo[r * ldd + k] = to_tf32(a - h);
+    }
+}
+
+// Operands of a complex (c64) product in real form, TF32 head/tail, K-major
+// with K' = 2 Kc:
+//   A' row r = [Re A(r, 0..Kc) | Im A(r, 0..Kc)]          (A column-major, ks)
+//   X' row 2j = [Re X(.., j) | -Im X(.., j)],  row 2j+1 = [Im X(.., j) | Re X(.., j)]
+//                                                          (X row-major, ks)
+// so that A' X'^T gives Re(A X) in column 2j and Im(A X) in column 2j+1.
+__global__ void split_c64_a_kernel(const float2 *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
+                                   float *__restrict__ hi, float *__restrict__ lo) {
+    __shared__ float2 tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + threadIdx.x, k = k0 + q;
+        tile[q][threadIdx.x] = (r < R && k < Kc) ? src[r + k * ks] : make_float2(0.f, 0.f);
+    }
+    __syncthreads();
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + q, k = k0 + threadIdx.x;
+        if (r < R && k < Kc) {
+            const float2 a = tile[threadIdx.x][q];
+            const int64_t o = r * 2 * Kc + k;
+            float h = to_tf32(a.x);
+            hi[o] = h;
+            lo[o] = to_tf32(a.x - h);
+            h = to_tf32(a.y);
+            hi[o + Kc] = h;
+            lo[o + Kc] = to_tf32(a.y - h);
+        }
+    }
+}
+
+__global__ void split_c64_x_kernel(const float2 *__restrict__ src, int64_t ks, int64_t Kc, int64_t N,
+                                   float *__restrict__ hi, float *__restrict__ lo) {
+    __shared__ float2 tile[32][33];
+    const int64_t j0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t j = j0 + threadIdx.x, k = k0 + q;
+        tile[q][threadIdx.x] = (j < N && k < Kc) ? src[k * ks + j] : make_float2(0.f, 0.f);
+    }
+    __syncthreads();
+    auto put = [&](int64_t o, float x) {
+        const float h = to_tf32(x);
+        hi[o] = h;
+        lo[o] = to_tf32(x - h);
+    };
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t j = j0 + q, k = k0 + threadIdx.x;
+        if (j < N && k < Kc) {
+            const float2 x = tile[threadIdx.x][q];
+            const int64_t re = 2 * j * 2 * Kc, im = re + 2 * Kc;
+            put(re + k, x.x);
+            put(re + Kc + k, -x.y);
+            put(im + k, x.y);
+            put(im + Kc + k, x.x);
         }
     }
 }
