@@ -45,10 +45,10 @@ TORCH_NAME = {"f32": "float32", "f64": "float64", "c64": "complex64", "c128": "c
 SQUARE = dict(m=64, n=64, batch=4096)
 # the kernel that solves the square64 batch of each type, and its key in
 # profiles/traffic.json
-SQUARE_KERNEL = {"f32": "small_pipe_f32_kernel<64>", "f64": "small_fast_kernel<double, 64, 64, 1, 64, 2>",
-                 "c64": "small_fast_kernel<float2, 64, 64, 1, 64, 2>",
-                 "c128": "small_fast_kernel<double2, 64, 64, 1, 32, 2>"}
-SQUARE_TRAFFIC_KEY = {"f32": "small_pipe_f32_kernel", "f64": "small_fast_kernel<f64>",
+SQUARE_KERNEL = {"f32": "small_tma_f32_kernel<64, 2>", "f64": "small_fast_kernel<double, 64, 64, 1, 32, 2>",
+                 "c64": "small_fast_kernel<float2, 64, 64, 1, 16, 2>",
+                 "c128": "small_fast_kernel<double2, 64, 64, 1, 16, 2>"}
+SQUARE_TRAFFIC_KEY = {"f32": "small_tma_f32_kernel", "f64": "small_fast_kernel<f64>",
                       "c64": "small_fast_kernel<c64>", "c128": "small_fast_kernel<c128>"}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
 FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike)

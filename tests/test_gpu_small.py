@@ -187,3 +187,13 @@ def test_persistent_f32_strided_layouts(env, m, geom):
     else:
         _parity(env, "f32", L, B, 1.0, f"{geom} m={m}", **kw)
     assert env["tg"].trsm_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f64", "c128"])
+@pytest.mark.parametrize("m,n,batch", [(64, 64, 1), (64, 100, 3), (16, 64, 40), (48, 9, 7), (32, 200, 2)])
+def test_fp64_few_systems_spread_columns(env, dtype, m, n, batch):
+    """FP64 batches too small to fill the GPU: the columns of each system go
+    to separate CTAs (slices of 1 to 8 columns, ragged last slice)."""
+    L, B = ti.generate(dtype, m, n, batch, kind="dd64", seed=m * n + batch)
+    alpha = (0.75 + 0.5j) if ti.IS_COMPLEX[dtype] else 0.75
+    _parity(env, dtype, L, B, alpha, f"spread {dtype} m={m} n={n} batch={batch}")

@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "small_kernels.cuh"
+#include "small_launch.cuh"
 #include "mbarrier.cuh"
 
 namespace trsm {
@@ -859,6 +860,18 @@ static int launch_fast_m(const SmallGeom &g, T alpha, cudaStream_t st) {
         }
         if (g.n <= 32) return launch_reg_f32<M, 32>(g, alpha, st);
         return launch_reg_f32<M, 64>(g, alpha, st);
+    }
+    if constexpr (std::is_same<T, double>::value || std::is_same<T, double2>::value) {
+        // too few systems to occupy every SM: spread their columns instead
+        // (a whole system on one SM is bound by that SM's FP64 rate)
+        static int sms = 0;
+        if (sms == 0) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (sms <= 0) sms = 152;
+        }
+        if (g.batch * ((g.n + 63) / 64) < 2 * sms) return launch_rowlane_split_m<T, M>(g, alpha, sms, st);
     }
     constexpr int CPT = std::is_same<T, float>::value ? 2 : 1;
     // row chunk: 16 rows for the complex types, 32 for f64; only the chunk's

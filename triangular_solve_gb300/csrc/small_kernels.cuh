@@ -260,13 +260,16 @@ __global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, c
     const int per = SmallImage<T, M>::elems(NC);
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int n = g.n;
+    // blockIdx.y picks a slice of NC columns: a launch with gridDim.y > 1
+    // spreads the columns of a few systems over many SMs
+    const int j0 = blockIdx.y * NC;
+    const int n = min(NC, g.n - j0);  // columns of this CTA
     const int64_t sys0 = (int64_t)blockIdx.x * g.spc;
     const int nsys = (int)min((int64_t)g.spc, g.batch - sys0);
 
     for (int s = 0; s < nsys; ++s) {
         T *Ls = base + s * per;
-        stage_system<T, M>(g, Ls, Ls + SmallImage<T, M>::kLs, Ls + SmallImage<T, M>::kLs + M, sys0 + s, 0, n,
+        stage_system<T, M>(g, Ls, Ls + SmallImage<T, M>::kLs, Ls + SmallImage<T, M>::kLs + M, sys0 + s, j0, n,
                            tid, nthr);
     }
     cp_async_wait_all();
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(128) small_rowlane_kernel(const SmallGeom g, c
     __syncthreads();
 
     for (int q = 0; q < nsys; ++q)
-        unstage_system<T, M>(g, base + q * per + SmallImage<T, M>::kLs + M, sys0 + q, 0, n, tid, nthr);
+        unstage_system<T, M>(g, base + q * per + SmallImage<T, M>::kLs + M, sys0 + q, j0, n, tid, nthr);
 }
 
 // ---------------------------------------------------------------- alpha == 0

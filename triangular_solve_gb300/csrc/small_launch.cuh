@@ -37,6 +37,32 @@ static int launch_rowlane(SmallGeom g, T alpha, cudaStream_t st) {
     return launch_status();
 }
 
+// Columns spread over CTAs: one warp per (system, NC-column slice).  For
+// FP64 batches too small to fill the GPU with whole systems, where a system
+// on one SM would be bound by that SM's FP64 rate.
+template <typename T, int M, int NC>
+static int launch_rowlane_split(SmallGeom g, T alpha, cudaStream_t st) {
+    g.spc = 1;
+    g.w = NC;
+    const size_t smem = SmallImage<T, M>::elems(NC) * sizeof(T);
+    auto kern = small_rowlane_kernel<T, M, NC>;
+    int rc = set_smem(kern, smem);
+    if (rc) return rc;
+    const dim3 grid((unsigned)g.batch, (unsigned)((g.n + NC - 1) / NC));
+    kern<<<grid, 32, smem, st>>>(g, alpha);
+    return launch_status();
+}
+
+// NC as large as keeps at least two CTAs per SM (else 1).
+template <typename T, int M>
+static int launch_rowlane_split_m(const SmallGeom &g, T alpha, int sms, cudaStream_t st) {
+    auto slices = [&](int nc) { return g.batch * ((g.n + nc - 1) / nc); };
+    if (slices(8) >= 2 * sms) return launch_rowlane_split<T, M, 8>(g, alpha, st);
+    if (slices(4) >= 2 * sms) return launch_rowlane_split<T, M, 4>(g, alpha, st);
+    if (slices(2) >= 2 * sms) return launch_rowlane_split<T, M, 2>(g, alpha, st);
+    return launch_rowlane_split<T, M, 1>(g, alpha, st);
+}
+
 template <typename T, int M>
 static int launch_colreg_m(SmallGeom g, T alpha, cudaStream_t st) {
     const int w = g.n < 64 ? g.n : 64;
