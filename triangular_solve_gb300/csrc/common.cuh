@@ -101,6 +101,12 @@ __device__ __forceinline__ C recip_smith(R c, R d) {
 __device__ __forceinline__ float2 recip(float2 d) { return recip_smith<float2, float>(d.x, d.y); }
 __device__ __forceinline__ double2 recip(double2 d) { return recip_smith<double2, double>(d.x, d.y); }
 
+// v == 1 exactly
+__device__ __forceinline__ bool is_one(float v) { return v == 1.f; }
+__device__ __forceinline__ bool is_one(double v) { return v == 1.0; }
+__device__ __forceinline__ bool is_one(float2 v) { return v.x == 1.f && v.y == 0.f; }
+__device__ __forceinline__ bool is_one(double2 v) { return v.x == 1.0 && v.y == 0.0; }
+
 template <typename T> __device__ __forceinline__ T ldg(const T *p) { return __ldg(p); }
 
 // ----------------------------------------------------------------------------

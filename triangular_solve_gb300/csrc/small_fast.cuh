@@ -84,19 +84,31 @@ struct FastDiag {
 template <typename T, int M, int RC, int CPT, int CH>
 struct FastChunks {
     static __device__ __forceinline__ void run(const T *__restrict__ Ls, const T *__restrict__ dinv, T *(&bs)[CPT],
-                                               T *(&gout)[CPT], const T alpha) {
+                                               T *(&gout)[CPT], const T alpha, const bool alpha_one) {
         if constexpr (CH < M / RC) {
             constexpr int V = Vec<T>::kN;
             T b[CPT][RC];
+            if (alpha_one) {  // uniform: no multiply at all (3% of the FP64 work)
 #pragma unroll
-            for (int c = 0; c < CPT; ++c)
+                for (int c = 0; c < CPT; ++c)
 #pragma unroll
-                for (int g0 = 0; g0 < RC; g0 += V) {
-                    T v[V];
-                    lds16<T>(bs[c] + CH * RC + g0, v);
+                    for (int g0 = 0; g0 < RC; g0 += V) {
+                        T v[V];
+                        lds16<T>(bs[c] + CH * RC + g0, v);
 #pragma unroll
-                    for (int u = 0; u < V; ++u) b[c][g0 + u] = mul(alpha, v[u]);
-                }
+                        for (int u = 0; u < V; ++u) b[c][g0 + u] = v[u];
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPT; ++c)
+#pragma unroll
+                    for (int g0 = 0; g0 < RC; g0 += V) {
+                        T v[V];
+                        lds16<T>(bs[c] + CH * RC + g0, v);
+#pragma unroll
+                        for (int u = 0; u < V; ++u) b[c][g0 + u] = mul(alpha, v[u]);
+                    }
+            }
             // rows solved by earlier chunks: a rolled loop (unrolled by 4),
             // so the code stays small enough for the instruction cache
 #pragma unroll 4
@@ -120,7 +132,7 @@ struct FastChunks {
                     if (CH + 1 < M / RC) *reinterpret_cast<float4 *>(bs[c] + CH * RC + g0) = v;
                 }
             }
-            FastChunks<T, M, RC, CPT, CH + 1>::run(Ls, dinv, bs, gout, alpha);
+            FastChunks<T, M, RC, CPT, CH + 1>::run(Ls, dinv, bs, gout, alpha, alpha_one);
         }
     }
 };
@@ -741,7 +753,7 @@ __global__ void __launch_bounds__(SPC *(W / CPT)) small_fast_kernel(const SmallG
     if constexpr (std::is_same<T, float>::value && CPT == 2 && RC == M)
         fast_solve_f32x2<M, CPT>(Ls, dinv, bs, gout, alpha);
     else
-        FastChunks<T, M, RC, CPT, 0>::run(Ls, dinv, bs, gout, alpha);
+        FastChunks<T, M, RC, CPT, 0>::run(Ls, dinv, bs, gout, alpha, is_one(alpha));
 }
 
 }  // namespace trsm
@@ -756,7 +768,10 @@ static int launch_fast_mw(const SmallGeom &g, T alpha, cudaStream_t st) {
     constexpr size_t per = (size_t)FastImage<T, M, W>::kElems * sizeof(T);
     constexpr int SPC_T = 128 / G > 0 ? 128 / G : 1;               // ~128 threads per CTA
     constexpr int SPC_S = (int)((220 * 1024) / per) > 0 ? (int)((220 * 1024) / per) : 1;
-    constexpr int SPC = SPC_T < SPC_S ? SPC_T : SPC_S;
+    // FP64 types: one system per CTA, so that the scheduler balances the
+    // last wave system by system (several CTAs share an SM)
+    constexpr bool kFp64 = std::is_same<T, double>::value || std::is_same<T, double2>::value;
+    constexpr int SPC = kFp64 ? 1 : (SPC_T < SPC_S ? SPC_T : SPC_S);
     constexpr size_t smem = (size_t)SPC * per;
     static_assert(smem <= 227 * 1024, "fast small kernel shared memory");
     auto kern = small_fast_kernel<T, M, W, CPT, RC, SPC>;
