@@ -129,7 +129,7 @@ struct FastChunks {
 #pragma unroll
                     for (int u = 0; u < V; ++u) e[u] = b[c][g0 + u];
                     *reinterpret_cast<float4 *>(gout[c] + CH * RC + g0) = v;
-                    if (CH + 1 < M / RC) *reinterpret_cast<float4 *>(bs[c] + CH * RC + g0) = v;
+                    if (CH + 1 < M / RC && bs[c] != gout[c]) *reinterpret_cast<float4 *>(bs[c] + CH * RC + g0) = v;
                 }
             }
             FastChunks<T, M, RC, CPT, CH + 1>::run(Ls, dinv, bs, gout, alpha, alpha_one);
@@ -694,11 +694,24 @@ __global__ void __launch_bounds__(TmaUnits<WPI>::kThreads, 1)
 
 // CTA: SPC systems x (W / CPT) threads each.  Thread g of a system owns
 // columns g + c*(W/CPT), c < CPT, of the CTA's column slice.
+// Shared image of a system whose RHS stays in global memory: packed L and the
+// reciprocal diagonal, rounded up to 16 bytes.
+template <typename T, int M>
+constexpr int fast_direct_image() {
+    constexpr int V = Vec<T>::kN;
+    return (Packed<T, M>::kSize + M + V - 1) / V * V;
+}
+
 template <typename T, int M, int W, int CPT, int RC, int SPC>
 __global__ void __launch_bounds__(SPC *(W / CPT)) small_fast_kernel(const SmallGeom g, const T alpha) {
     using Img = FastImage<T, M, W>;
     using P = Packed<T, M>;
     constexpr int V = Img::V;
+    // FP64 types read their RHS straight from global memory, chunk by chunk
+    // (the FP64 rate hides the latency), so a system needs only L on chip
+    // and several systems share an SM
+    constexpr bool kDirect = std::is_same<T, double>::value || std::is_same<T, double2>::value;
+    constexpr int kImg = kDirect ? fast_direct_image<T, M>() : Img::kElems;
     constexpr int G = W / CPT;           // threads per system
     constexpr int NT = SPC * G;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -715,13 +728,13 @@ __global__ void __launch_bounds__(SPC *(W / CPT)) small_fast_kernel(const SmallG
     for (int cidx = warp; cidx < nsys * M; cidx += NWARPS) {
         const int s = cidx / M, k = cidx - s * M;
         const T *src = Ag + (sys0 + s) * g.sA + (int64_t)k * g.lda + P::s(k);
-        T *dst = base + s * Img::kElems + P::off(k);
+        T *dst = base + s * kImg + P::off(k);
         const int nch = (M - P::s(k)) / V;
         for (int q = lane; q < nch; q += 32) cp_async<16>(dst + q * V, src + q * V);
     }
     // RHS slice: flat 16-byte chunks; columns past n are zero-filled
     constexpr int CH_PER_COL = M / V;
-    for (int e = tid; e < nsys * W * CH_PER_COL; e += NT) {
+    for (int e = tid; !kDirect && e < nsys * W * CH_PER_COL; e += NT) {
         const int s = e / (W * CH_PER_COL), r = e - s * (W * CH_PER_COL);
         const int j = r / CH_PER_COL, q = r - j * CH_PER_COL;
         T *dst = base + s * Img::kElems + Img::kLs + M + j * Img::kBld + q * V;
@@ -733,23 +746,24 @@ __global__ void __launch_bounds__(SPC *(W / CPT)) small_fast_kernel(const SmallG
     // reciprocals of the diagonal (row k of packed column k)
     for (int e = tid; e < nsys * M; e += NT) {
         const int s = e / M, k = e - s * M;
-        T *img = base + s * Img::kElems;
+        T *img = base + s * kImg;
         img[Img::kLs + k] = recip(img[P::off(k) + (k - P::s(k))]);
     }
     __syncthreads();
 
     const int s = tid / G, gi = tid - s * G;
     if (s >= nsys) return;
-    const T *Ls = base + s * Img::kElems;
+    const T *Ls = base + s * kImg;
     const T *dinv = Ls + Img::kLs;
     T *bs[CPT];
     T *gout[CPT];
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
         const int j = gi + c * G;
-        bs[c] = base + s * Img::kElems + Img::kLs + M + j * Img::kBld;
         gout[c] = (j0 + j < g.n) ? Bg + (sys0 + s) * g.sB + (int64_t)(j0 + j) * g.ldb : nullptr;
+        bs[c] = kDirect ? gout[c] : base + s * Img::kElems + Img::kLs + M + j * Img::kBld;
     }
+    if (kDirect && gout[0] == nullptr) return;  // one column per thread: past n
     if constexpr (std::is_same<T, float>::value && CPT == 2 && RC == M)
         fast_solve_f32x2<M, CPT>(Ls, dinv, bs, gout, alpha);
     else
@@ -765,13 +779,14 @@ constexpr int kFastNotApplicable = -100000;
 template <typename T, int M, int W, int CPT, int RC>
 static int launch_fast_mw(const SmallGeom &g, T alpha, cudaStream_t st) {
     constexpr int G = W / CPT;
-    constexpr size_t per = (size_t)FastImage<T, M, W>::kElems * sizeof(T);
+    constexpr bool kDirect = std::is_same<T, double>::value || std::is_same<T, double2>::value;
+    constexpr size_t per =
+        (size_t)(kDirect ? fast_direct_image<T, M>() : FastImage<T, M, W>::kElems) * sizeof(T);
     constexpr int SPC_T = 128 / G > 0 ? 128 / G : 1;               // ~128 threads per CTA
     constexpr int SPC_S = (int)((220 * 1024) / per) > 0 ? (int)((220 * 1024) / per) : 1;
     // FP64 types: one system per CTA, so that the scheduler balances the
     // last wave system by system (several CTAs share an SM)
-    constexpr bool kFp64 = std::is_same<T, double>::value || std::is_same<T, double2>::value;
-    constexpr int SPC = kFp64 ? 1 : (SPC_T < SPC_S ? SPC_T : SPC_S);
+    constexpr int SPC = kDirect ? 1 : (SPC_T < SPC_S ? SPC_T : SPC_S);
     constexpr size_t smem = (size_t)SPC * per;
     static_assert(smem <= 227 * 1024, "fast small kernel shared memory");
     auto kern = small_fast_kernel<T, M, W, CPT, RC, SPC>;
