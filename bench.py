@@ -438,7 +438,7 @@ def nb_sweep(args):
             b0 = bv.to(t).t().contiguous().t()
             del lv, bv
             best = None
-            for nb in (128, 256, 512):
+            for nb in [int(x) for x in args.sweep_nbs.split(",")]:
                 wsb = tg.trsm_llnn_workspace_bytes(d, mm, mm, nb)
                 wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
                 b = b0.clone()
@@ -560,6 +560,7 @@ def main():
     ap.add_argument("--sweep-dtypes", default="f32,f64,c64,c128")
     ap.add_argument("--sweep-ms", default="1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-reps", type=int, default=3)
+    ap.add_argument("--sweep-nbs", default="128,256,512", help="block sizes of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtypes", default="f32,f64,c64,c128",
                     help="subset of the step's types (profiling a single kernel)")
