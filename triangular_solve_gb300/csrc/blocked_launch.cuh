@@ -248,6 +248,25 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
                 continue;
             }
         }
+        if constexpr (std::is_same<T, float2>::value) {
+            // the same with the complex products in real form
+            const bool has_update = r0 + nb < m;
+            if (tc_panels && tc_apply_usable_c64(mb, n) &&
+                (!has_update || tc_update_usable(m - r0 - nb, 2 * n, 2 * nb))) {
+                timer.begin();
+                rc = tc_apply_c64(mb, n, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
+                if (rc || (rc = timer.end(1))) return rc;
+                timer.begin();
+                if (has_update) {
+                    const T beta = (t == 0) ? alpha : one;
+                    rc = tc_update_c64(m - r0 - nb, n, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
+                                       a.ldb, beta, m, tc_panels, st);
+                    if (rc) return rc;
+                }
+                if ((rc = timer.end(2))) return rc;
+                continue;
+            }
+        }
         timer.begin();
         rc = kSpNotApplicable;
         if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {

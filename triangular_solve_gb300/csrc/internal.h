@@ -68,8 +68,9 @@ inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 // f32 adds the TF32 head/tail panels of the tensor-core products
 // (tc_panel_bytes: the A operand -- L panel or D_t^-1 --, the X operand and
 // the split X_t the apply leaves for the update, two copies each, K-major).
-// c64 adds the real-form operands of its tensor-core update
-// (tc_panel_bytes_c64: A' = m x 2nb, X' = 2n x 2nb, two copies each).
+// c64 adds the real-form operands of its tensor-core products
+// (tc_panel_bytes_c64: A' = m x 2nb, X' = 2n x 2nb and the split X_t' the
+// apply leaves for the update, two copies each).
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb);
 size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb);
 inline size_t blocked_workspace_bytes(int dtype, int64_t m, int64_t n, int64_t nb) {
@@ -88,6 +89,9 @@ bool tc_update_usable(int64_t M, int64_t N, int64_t K);
 bool tc_apply_usable(int64_t mb, int64_t N);
 int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *X, int64_t ldx,
                   float *C, int64_t ldc, float beta, int64_t Mmax, void *panels, cudaStream_t st);
+bool tc_apply_usable_c64(int64_t mb, int64_t N);
+int tc_apply_c64(int64_t mb, int64_t N, const float2 *Wt, int64_t nb, float2 *Bt, int64_t ldb, float2 gamma,
+                 int64_t Mmax, void *panels, bool emit_split, cudaStream_t st);
 int tc_update_c64(int64_t M, int64_t N, int64_t K, const float2 *A, int64_t lda, const float2 *X, int64_t ldx,
                   float2 *C, int64_t ldc, float2 beta, int64_t Mmax, void *panels, cudaStream_t st);
 int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, int64_t ldb, float gamma,

@@ -180,6 +180,7 @@ TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
     g.beta = 0.f;
     g.beta_im = 0.f;
     g.gamma = -1.f;
+    g.gamma_im = 0.f;
     g.beta_zero = 0;
     g.a_lower = 0;
     g.cplx = 0;
@@ -212,31 +213,87 @@ int tc_update_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
     return launch_tc(p.a_hi, p.a_lo, xh, xl, g, st);
 }
 
-// c64 trailing update C = beta*C - A X (A column-major lda, X the row-major
-// panel, ldx, all complex) as one real product of M x 2N x 2K on the
-// tensor cores (see split_c64_*).  Panels: tc_panel_bytes_c64(Mmax, N, K).
+// c64 panels: A' (Mmax x 2nb), X' (2N x 2nb), and the split X_t' the complex
+// apply leaves for the update, head and tail each.
+struct TcPanelsC64 {
+    float *a_hi, *a_lo, *x_hi, *x_lo, *xs_hi, *xs_lo;
+};
+
+static TcPanelsC64 tc_layout_c64(void *panels, int64_t m, int64_t n, int64_t nb) {
+    TcPanelsC64 p;
+    char *c = static_cast<char *>(panels);
+    const size_t A = round256(m * 2 * nb * 4), X = round256(2 * n * 2 * nb * 4);
+    p.a_hi = reinterpret_cast<float *>(c);
+    p.a_lo = reinterpret_cast<float *>(c + A);
+    p.x_hi = reinterpret_cast<float *>(c + 2 * A);
+    p.x_lo = reinterpret_cast<float *>(c + 2 * A + X);
+    p.xs_hi = reinterpret_cast<float *>(c + 2 * A + 2 * X);
+    p.xs_lo = reinterpret_cast<float *>(c + 2 * A + 3 * X);
+    return p;
+}
+
+size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb) {
+    return (size_t)(2 * round256(m * 2 * nb * 4) + 4 * round256(2 * n * 2 * nb * 4));
+}
+
+// c64 trailing update C = beta*C - A X (A column-major lda, all complex) as
+// one real product of M x 2N x 2K on the tensor cores (see split_c64_*).
+// X is the row-major panel (ldx), split here, or -- X == nullptr -- the split
+// copy tc_apply_c64 left in the panels (tc_panel_bytes_c64(Mmax, N, K)).
 int tc_update_c64(int64_t M, int64_t N, int64_t K, const float2 *A, int64_t lda, const float2 *X, int64_t ldx,
                   float2 *C, int64_t ldc, float2 beta, int64_t Mmax, void *panels, cudaStream_t st) {
-    char *c = static_cast<char *>(panels);
-    const size_t Ab = round256(Mmax * 2 * K * 4), Xb = round256(2 * N * 2 * K * 4);
-    float *a_hi = reinterpret_cast<float *>(c), *a_lo = reinterpret_cast<float *>(c + Ab);
-    float *x_hi = reinterpret_cast<float *>(c + 2 * Ab), *x_lo = reinterpret_cast<float *>(c + 2 * Ab + Xb);
+    const TcPanelsC64 p = tc_layout_c64(panels, Mmax, N, K);
     split_c64_a_kernel<<<dim3((unsigned)((M + 31) / 32), (unsigned)((K + 31) / 32)), dim3(32, 8), 0, st>>>(
-        A, lda, M, K, a_hi, a_lo);
+        A, lda, M, K, p.a_hi, p.a_lo);
     int rc = launch_status();
     if (rc) return rc;
-    split_c64_x_kernel<<<dim3((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32)), dim3(32, 8), 0, st>>>(
-        X, ldx, K, N, x_hi, x_lo);
-    if ((rc = launch_status())) return rc;
+    const float *xh = p.xs_hi, *xl = p.xs_lo;
+    if (X) {
+        split_c64_x_kernel<<<dim3((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32)), dim3(32, 8), 0, st>>>(
+            X, ldx, K, N, p.x_hi, p.x_lo);
+        if ((rc = launch_status())) return rc;
+        xh = p.x_hi;
+        xl = p.x_lo;
+    }
     TcArgs g = tc_args(M, 2 * N, 2 * K, reinterpret_cast<float *>(C), 2 * ldc);
     g.beta = beta.x;
     g.beta_im = beta.y;
     g.cplx = 1;
-    return launch_tc(a_hi, a_lo, x_hi, x_lo, g, st);
+    return launch_tc(p.a_hi, p.a_lo, xh, xl, g, st);
 }
 
-size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb) {
-    return (size_t)(2 * round256(m * 2 * nb * 4) + 2 * round256(2 * n * 2 * nb * 4));
+bool tc_apply_usable_c64(int64_t mb, int64_t N) {
+    const int64_t tiles = ((mb + TC_BM - 1) / TC_BM) * ((2 * N + TC_BN - 1) / TC_BN);
+    return tc_update_usable(mb, 2 * N, 2 * mb) && tiles >= 48;
+}
+
+// Complex block apply on the tensor cores: X_t = gamma * D_t^-1 R_t over R_t
+// (block row of B, column-major ldb), D_t^-1 the column-major lower-
+// triangular block Wt (ld nb); real form with interleaved K' so the
+// triangular K range stays a prefix.  With emit_split the epilogue leaves
+// X_t' split for tc_update_c64 (X == nullptr).
+int tc_apply_c64(int64_t mb, int64_t N, const float2 *Wt, int64_t nb, float2 *Bt, int64_t ldb, float2 gamma,
+                 int64_t Mmax, void *panels, bool emit_split, cudaStream_t st) {
+    const TcPanelsC64 p = tc_layout_c64(panels, Mmax, N, nb);
+    split_c64_ai_kernel<<<dim3((unsigned)((mb + 31) / 32), (unsigned)((mb + 31) / 32)), dim3(32, 8), 0, st>>>(
+        Wt, nb, mb, mb, p.a_hi, p.a_lo);
+    int rc = launch_status();
+    if (rc) return rc;
+    split_c64_xi_kernel<<<dim3((unsigned)((mb + 127) / 128), (unsigned)(N < 65535 ? N : 65535)), 128, 0, st>>>(
+        Bt, ldb, mb, N, p.x_hi, p.x_lo);
+    if ((rc = launch_status())) return rc;
+    TcArgs g = tc_args(mb, 2 * N, 2 * mb, reinterpret_cast<float *>(Bt), 2 * ldb);
+    g.beta_zero = 1;
+    g.gamma = gamma.x;
+    g.gamma_im = gamma.y;
+    g.a_lower = 2;
+    g.cplx = 1;
+    if (emit_split) {
+        g.xhi = p.xs_hi;
+        g.xlo = p.xs_lo;
+        g.ldxs = 2 * nb;
+    }
+    return launch_tc(p.a_hi, p.a_lo, p.x_hi, p.x_lo, g, st);
 }
 
 // Block apply on the tensor cores: X_t = gamma * D_t^-1 R_t, written over

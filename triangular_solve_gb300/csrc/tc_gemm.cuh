@@ -47,14 +47,18 @@ constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYT
 // stored to C; with xhi set, out is also stored split (TF32 head/tail) and
 // K-major, xhi[col * ldxs + row], as the X operand of a later product.
 // a_lower: A is lower triangular, so a row tile stops its K loop at its last
-// row.  cplx: the product is the real form of a complex one, output columns
-// 2j and 2j+1 being the real and imaginary parts of complex column j of C
-// (interleaved, ldc counted in floats), and beta = beta + i*beta_im.
+// row (a_lower = 2: K interleaves real and imaginary parts, two K per row).
+// cplx: the product is the real form of a complex one, output columns 2j
+// and 2j+1 being the real and imaginary parts of complex column j of C
+// (interleaved, ldc counted in floats); beta = beta + i*beta_im and
+// gamma = gamma + i*gamma_im multiply complex values; with xhi set the
+// split copy is the X' operand of tc_update_c64: row 2j = [Re | -Im],
+// row 2j+1 = [Im | Re], halves ldxs/2 apart.
 struct TcArgs {
     int64_t M, N, K;
     float *C;
     int64_t ldc;
-    float beta, beta_im, gamma;
+    float beta, beta_im, gamma, gamma_im;
     int beta_zero, a_lower, cplx;
     float *xhi, *xlo;
     int64_t ldxs;
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(192, 1)
             int it = 0;
             for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
                 const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
-                const int nkt = g.a_lower ? min(nk, (m0 + TC_BM) / TC_BK) : nk;
+                const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
                 for (int kb = 0; kb < nkt; ++kb, ++it) {
                     const int s = it % TC_STAGES;
                     if (it >= TC_STAGES && !mbar_wait(empty(s), ((it / TC_STAGES) - 1) & 1)) {
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(192, 1)
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(a * TC_BN);
                 const int m0 = (t % tiles_m) * TC_BM;
-                const int nkt = g.a_lower ? min(nk, (m0 + TC_BM) / TC_BK) : nk;
+                const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
                 bool ok = true;
                 for (int kb = 0; kb < nkt; ++kb, ++it) {
                     const int s = it % TC_STAGES;
@@ -304,10 +308,24 @@ __global__ void __launch_bounds__(192, 1)
                         const int64_t gc = n0 + chunk * 32 + j;  // even: a (re, im) pair
                         if (gc < g.N) {
                             const float cr = ccur[j], ci = ccur[j + 1];
-                            const float ar = g.gamma * __uint_as_float(v[j]), ai = g.gamma * __uint_as_float(v[j + 1]);
+                            const float pr = __uint_as_float(v[j]), pi = __uint_as_float(v[j + 1]);
+                            const float ar = fmaf(g.gamma, pr, -g.gamma_im * pi);
+                            const float ai = fmaf(g.gamma, pi, g.gamma_im * pr);
                             const float orr = fmaf(g.beta, cr, fmaf(-g.beta_im, ci, ar));
                             const float oi = fmaf(g.beta, ci, fmaf(g.beta_im, cr, ai));
                             *reinterpret_cast<float2 *>(g.C + coff(gc)) = make_float2(orr, oi);
+                            if (g.xhi) {
+                                const int64_t re_row = gc * g.ldxs, im_row = re_row + g.ldxs, half = g.ldxs / 2;
+                                auto put = [&](int64_t o, float x) {
+                                    const float h = to_tf32(x);
+                                    g.xhi[o] = h;
+                                    g.xlo[o] = to_tf32(x - h);
+                                };
+                                put(re_row + gr, orr);
+                                put(re_row + half + gr, -oi);
+                                put(im_row + gr, oi);
+                                put(im_row + half + gr, orr);
+                            }
                         }
                     }
                 } else if (row_ok) {
@@ -430,6 +448,49 @@ __global__ void split_c64_x_kernel(const float2 *__restrict__ src, int64_t ks, i
             put(im + k, x.y);
             put(im + Kc + k, x.x);
         }
+    }
+}
+
+// Operands of the complex block apply in real form with interleaved K'
+// (k' = 2k for the real part, 2k + 1 for the imaginary part), which keeps a
+// lower-triangular A's K range a prefix:
+//   A' row r = [Re A(r,0), Im A(r,0), Re A(r,1), ...]   (A column-major, ks)
+//   X' row 2j = [Re X(0,j), -Im X(0,j), ...], row 2j+1 = [Im X(0,j), Re X(0,j), ...]
+//                                                      (X column-major, ks)
+__global__ void split_c64_ai_kernel(const float2 *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
+                                    float *__restrict__ hi, float *__restrict__ lo) {
+    __shared__ float2 tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + threadIdx.x, k = k0 + q;
+        tile[q][threadIdx.x] = (r < R && k < Kc) ? src[r + k * ks] : make_float2(0.f, 0.f);
+    }
+    __syncthreads();
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t r = r0 + q, k = k0 + threadIdx.x;
+        if (r < R && k < Kc) {
+            const float2 a = tile[threadIdx.x][q];
+            const float hr = to_tf32(a.x), hi_ = to_tf32(a.y);
+            const int64_t o = r * 2 * Kc + 2 * k;
+            *reinterpret_cast<float2 *>(hi + o) = make_float2(hr, hi_);
+            *reinterpret_cast<float2 *>(lo + o) = make_float2(to_tf32(a.x - hr), to_tf32(a.y - hi_));
+        }
+    }
+}
+
+__global__ void split_c64_xi_kernel(const float2 *__restrict__ src, int64_t ks, int64_t Kc, int64_t N,
+                                    float *__restrict__ hi, float *__restrict__ lo) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= Kc) return;
+    for (int64_t j = blockIdx.y; j < N; j += gridDim.y) {
+        const float2 x = src[j * ks + k];
+        const float hr = to_tf32(x.x), hm = to_tf32(x.y);
+        const float lr = to_tf32(x.x - hr), lm = to_tf32(x.y - hm);
+        const int64_t re = 2 * j * 2 * Kc + 2 * k, im = re + 2 * Kc;
+        *reinterpret_cast<float2 *>(hi + re) = make_float2(hr, -hm);
+        *reinterpret_cast<float2 *>(lo + re) = make_float2(lr, -lm);
+        *reinterpret_cast<float2 *>(hi + im) = make_float2(hm, hr);
+        *reinterpret_cast<float2 *>(lo + im) = make_float2(lm, lr);
     }
 }
 
