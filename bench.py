@@ -45,13 +45,14 @@ TORCH_NAME = {"f32": "float32", "f64": "float64", "c64": "complex64", "c128": "c
 SQUARE = dict(m=64, n=64, batch=4096)
 # the kernel that solves the square64 batch of each type, and its key in
 # profiles/traffic.json
-SQUARE_KERNEL = {"f32": "small_tma_f32_kernel<64, 2>", "f64": "small_fast_kernel<double, 64, 64, 1, 32, 2>",
+SQUARE_KERNEL = {"f32": "small_tma_f32_kernel<64, 2>", "f64": "small_fast_kernel<double, 64, 64, 1, 32, 1>",
                  "c64": "small_fast_kernel<float2, 64, 64, 1, 16, 2>",
-                 "c128": "small_fast_kernel<double2, 64, 64, 1, 16, 2>"}
+                 "c128": "small_fast_kernel<double2, 64, 64, 1, 16, 1>"}
 SQUARE_TRAFFIC_KEY = {"f32": "small_tma_f32_kernel", "f64": "small_fast_kernel<f64>",
                       "c64": "small_fast_kernel<c64>", "c128": "small_fast_kernel<c128>"}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
 FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike)
+TF32_PEAK_TFLOPS = 1100.0        # nominal dense TF32 tensor rate; 3xTF32 costs three products
 SM_COUNT, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
 
 
@@ -395,10 +396,15 @@ def run_large(torch, tg, dev, stream, peaks, reps=2):
         gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
         tot = sum(phases)
         fp64 = d in ("f64", "c128")
+        # f32 / c64: the GEMMs run on the tensor cores as 3xTF32 products, whose
+        # f32-accurate ceiling is a third of the TF32 rate
+        peak = FP64_PEAK_TFLOPS if fp64 else TF32_PEAK_TFLOPS / 3
         res[f"{d}_m{mm}"] = {
             "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1),
-            "pipe": "FP64 (DFMA)" if fp64 else "FP32 (FFMA)",
-            "frac_of_pipe_peak": round(gf / 1e3 / (FP64_PEAK_TFLOPS if fp64 else fp32_alu_peak_tflops()), 4),
+            "pipe": "FP64 (DFMA)" if fp64 else "tensor (tcgen05 kind::tf32, 3xTF32)",
+            "peak_tflops": round(peak, 1),
+            "frac_of_pipe_peak": round(gf / 1e3 / peak, 4),
+            **({} if fp64 else {"frac_of_fp32_fma_peak": round(gf / 1e3 / fp32_alu_peak_tflops(), 4)}),
             "phase_share": {"diag_inversion": round(phases[0] / tot, 4),
                             "block_apply": round(phases[1] / tot, 4),
                             "gemm_update": round(phases[2] / tot, 4)},
