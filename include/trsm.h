@@ -98,6 +98,28 @@ int trsm_llnn_strided_batched(trsm_dtype_t dtype, trsm_layout_t layout, int64_t 
                               void *stream);
 
 /*
+ * trsm_llnn_strided_batched on HOST buffers: A and B are host pointers (page-
+ * locked memory lets the copies run asynchronously and overlap; pageable
+ * memory works but serialises them), same arguments, layouts, strides and
+ * validation as trsm_llnn_strided_batched.  B is overwritten with X.
+ * The pages describe no such entry point; it exists for callers whose data
+ * lives in host memory.
+ *
+ * The batch is cut into up to eight chunks that alternate between two
+ * internal streams: while one chunk is being solved, the next one is copied
+ * in and the previous one copied out.  Device buffers for two chunks come
+ * from cudaMallocAsync on `stream` and are released on it.  The call is
+ * stream-ordered like the others: it returns once the work is enqueued, and
+ * X is in B only when `stream` has reached the end of this call's work
+ * (synchronise it before reading B).  A and B must stay valid and B must not
+ * be read or written by the host until then.  Returns the first error of the
+ * copies or solves (TRSM_ERR_CUDA_BASE + cudaError_t, or the solve's status).
+ */
+int trsm_llnn_strided_batched_host(trsm_dtype_t dtype, trsm_layout_t layout, int64_t m, int64_t n,
+                                   const void *alpha, const void *A, int64_t lda, int64_t strideA,
+                                   void *B, int64_t ldb, int64_t strideB, int64_t batch, void *stream);
+
+/*
  * Block size NB the blocked path uses for (dtype, m, n): the entry of the
  * compile-time "size x type -> block size" table of the nearest tabulated m
  * ("Hierarchical Shared Memory-Aware Optimization for TRSM on GPU

@@ -15,7 +15,7 @@ def lib():
     return tg.load_library()
 
 
-EXPECTED = {"trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_select_nb",
+EXPECTED = {"trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
             "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string"}
 
 

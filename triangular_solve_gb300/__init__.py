@@ -66,6 +66,8 @@ def load_library():
         lib.trsm_llnn.argtypes = [i32, i64, i64, vp, vp, i64, vp, i64, vp]
         lib.trsm_llnn_strided_batched.argtypes = [i32, i32, i64, i64, vp, vp, i64, i64, vp, i64, i64,
                                                   i64, vp]
+        lib.trsm_llnn_strided_batched_host.argtypes = [i32, i32, i64, i64, vp, vp, i64, i64, vp, i64, i64,
+                                                       i64, vp]
         lib.trsm_llnn_select_nb.argtypes = [i32, i64, i64]
         lib.trsm_llnn_workspace_bytes.argtypes = [i32, i64, i64, i64]
         lib.trsm_llnn_workspace_bytes.restype = ctypes.c_size_t
@@ -74,7 +76,7 @@ def load_library():
                                           vp, ctypes.POINTER(ctypes.c_float)]
         lib.trsm_status_string.argtypes = [i32]
         lib.trsm_status_string.restype = ctypes.c_char_p
-        for name in ("trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_select_nb",
+        for name in ("trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
                      "trsm_llnn_ex", "trsm_llnn_profile"):
             getattr(lib, name).restype = i32
         _lib = lib
@@ -156,6 +158,25 @@ def trsm_llnn_strided_batched(dtype, layout, m, n, alpha, A, lda, strideA, B, ld
     al, _ = _alpha_buf(code, alpha)
     _check("trsm_llnn_strided_batched", load_library().trsm_llnn_strided_batched(
         code, _layout_code(layout), m, n, al, _ptr(A), lda, strideA, _ptr(B), ldb, strideB, batch,
+        _stream(stream)))
+
+
+def _host_ptr(x):
+    if hasattr(x, "data_ptr"):
+        if x.is_cuda:
+            raise ValueError("trsm_llnn_strided_batched_host takes host (CPU) tensors")
+        return x.data_ptr()
+    return x
+
+
+def trsm_llnn_strided_batched_host(dtype, layout, m, n, alpha, A, lda, strideA, B, ldb, strideB, batch,
+                                   stream=None) -> None:
+    """The strided-batched solve on host buffers (pinned CPU tensors for
+    overlapped copies); enqueued on `stream`, B holds X once it has run."""
+    code = _dtype_code(dtype)
+    al, _ = _alpha_buf(code, alpha)
+    _check("trsm_llnn_strided_batched_host", load_library().trsm_llnn_strided_batched_host(
+        code, _layout_code(layout), m, n, al, _host_ptr(A), lda, strideA, _host_ptr(B), ldb, strideB, batch,
         _stream(stream)))
 
 
