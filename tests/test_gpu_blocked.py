@@ -150,3 +150,18 @@ def test_tensor_core_products_ragged(env, dtype, nb, m, n):
     xg, xr = _ex_solve(env, dtype, L, B, alpha, nb, lda=m + 4, ldb=m + 8)
     assert env["tg"].trsm_device_status() == 0
     assert_parity(dtype, xg, xr, f"tc {dtype} m={m} n={n} nb={nb}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
+def test_batched_blocked_tensor_core_systems(env, dtype):
+    """Strided batch of m > 64 systems large enough for the tensor-core apply
+    and update, with padding between systems."""
+    m, n, batch = 640, 300, 2
+    L, B = ti.generate(dtype, m, n, batch, kind="ddm", seed=7)
+    a, b, geo = storage_pair(L, B, lda=m + 4, ldb=m + 8, stride_a=m * (m + 4) + 16, stride_b=n * (m + 8) + 32)
+    alpha = (0.5 + 0.25j) if ti.IS_COMPLEX[dtype] else 0.5
+    raw = gpu_solve_buffers(dtype, a, b, geo, alpha, env["torch"], env["tg"])
+    ref = oracle_buffers(dtype, a, b, geo, alpha, env["oracle"])
+    assert env["tg"].trsm_device_status() == 0
+    assert_padding_untouched(raw, b, geo)
+    assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"batched tc {dtype}")
