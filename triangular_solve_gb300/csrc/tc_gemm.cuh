@@ -36,11 +36,19 @@
 
 namespace trsm {
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 32, TC_STAGES = 2;
-constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 16 KB
-constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 32 KB
-constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 96 KB
+// K depth of a stage: 16 (64-byte rows, 64-byte swizzle, four stages) or 32
+// (128-byte rows and swizzle, two stages); the same 192 KB of ring either way,
+// but shallower stages let the producer run further ahead of the MMAs
+// (measured on GB300: 16 is 1.5-10% faster on the blocked solves).
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 16, TC_STAGES = TC_BK == 16 ? 4 : 2;
+static_assert(TC_BK == 16 || TC_BK == 32, "stage depth");
+constexpr uint32_t TC_ROW_BYTES = TC_BK * 4;                          // a K-major tile row: the swizzle span
+constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 8 / 16 KB
+constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 16 / 32 KB
+constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 48 / 96 KB
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column FP32 accumulators
+constexpr uint32_t kTmemSlotOffset = 8u * (2 * TC_STAGES + 5);  // after the 2*TC_STAGES + 5 barriers
+static_assert(kTmemSlotOffset + 4 <= 128, "barriers and TMEM slot fit the 128-byte region");
 constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
 
 // out = beta*C + gamma*(A X) (beta_zero: out = gamma*(A X), C not read),
@@ -73,15 +81,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
-// rows of 128 bytes (32 TF32 values), 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major tile with TC_ROW_BYTES-byte
+// rows and the matching swizzle (128 B: mode 2, 64 B: mode 4); 8-row groups
+// 8 * TC_ROW_BYTES apart.
+__device__ __forceinline__ uint64_t tile_desc(uint32_t saddr) {
     uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
-    d |= (uint64_t)1 << 16;                   // leading byte offset (unused when swizzled)
-    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: next 8-row group
-    d |= (uint64_t)1 << 46;                   // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);                  // start address
+    d |= (uint64_t)1 << 16;                                   // leading byte offset (unused when swizzled)
+    d |= (uint64_t)((8 * TC_ROW_BYTES) >> 4) << 32;           // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                                   // descriptor version for tcgen05
+    d |= (uint64_t)(TC_ROW_BYTES == 128 ? 2 : 4) << 61;       // swizzle mode
     return d;
 }
 
@@ -133,12 +142,13 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment for the swizzled tiles
     unsigned char *sbase = smem_raw + (base - raw);
     const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;
+    // barrier region: full[TC_STAGES], empty[TC_STAGES], acc_full[2], acc_empty[2], drain, then the TMEM slot
     auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 16u + 8u * s; };
-    auto acc_full = [&](int a) { return bars + 32u + 8u * a; };
-    auto acc_empty = [&](int a) { return bars + 48u + 8u * a; };
-    const uint32_t drain = bars + 64u;  // last commit of the MMA thread
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + 72);
+    auto empty = [&](int s) { return bars + 8u * (TC_STAGES + s); };
+    auto acc_full = [&](int a) { return bars + 8u * (2 * TC_STAGES + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (2 * TC_STAGES + 2 + a); };
+    const uint32_t drain = bars + 8u * (2 * TC_STAGES + 4);  // last commit of the MMA thread
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + kTmemSlotOffset);
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,10 +238,10 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t st = base + s * TC_STAGE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < TC_BK / 8; ++kk) {
-                        const uint64_t a_hi = sw128_desc(st + kk * 32);
-                        const uint64_t a_lo = sw128_desc(st + TC_A_BYTES + kk * 32);
-                        const uint64_t x_hi = sw128_desc(st + 2 * TC_A_BYTES + kk * 32);
-                        const uint64_t x_lo = sw128_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
+                        const uint64_t a_hi = tile_desc(st + kk * 32);
+                        const uint64_t a_lo = tile_desc(st + TC_A_BYTES + kk * 32);
+                        const uint64_t x_hi = tile_desc(st + 2 * TC_A_BYTES + kk * 32);
+                        const uint64_t x_lo = tile_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
                         mma_tf32(d, a_hi, x_hi, idesc, (kb | kk) != 0);
                         mma_tf32(d, a_hi, x_lo, idesc, 1);
                         mma_tf32(d, a_lo, x_hi, idesc, 1);
