@@ -42,6 +42,7 @@ namespace trsm {
 // (measured on GB300: 16 is 1.5-10% faster on the blocked solves).
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 16, TC_STAGES = TC_BK == 16 ? 4 : 2;
 static_assert(TC_BK == 16 || TC_BK == 32, "stage depth");
+constexpr int kTileGroup = 8;  // row tiles per group of the tile order
 constexpr uint32_t TC_ROW_BYTES = TC_BK * 4;                          // a K-major tile row: the swizzle span
 constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 8 / 16 KB
 constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 16 / 32 KB
@@ -154,6 +155,18 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = (int)((g.K + TC_BK - 1) / TC_BK);
     const int tiles_m = (int)((g.M + TC_BM - 1) / TC_BM);
+    const int tiles_n = (int)((g.N + TC_BN - 1) / TC_BN);
+    // Tile t -> (row tile, column tile), grouped: kTileGroup row tiles walk all
+    // column tiles together, so a wave of CTAs shares a few A tiles and a few
+    // X tiles in L2 instead of streaming the whole A panel once per column
+    // tile (the operand panels of large solves exceed L2).
+    auto tile_of = [&](int t, int &tm, int &tn) {
+        const int per = kTileGroup * tiles_n;
+        const int grp = t / per, rem = t - grp * per;
+        const int gsize = min(kTileGroup, tiles_m - grp * kTileGroup);
+        tm = grp * kTileGroup + rem % gsize;
+        tn = rem / gsize;
+    };
     const int ntiles = tiles_m * (int)((g.N + TC_BN - 1) / TC_BN);
 
     if (threadIdx.x == 0) {
@@ -189,7 +202,9 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
-                const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
+                int tm, tn;
+                tile_of(t, tm, tn);
+                const int m0 = tm * TC_BM, n0 = tn * TC_BN;
                 const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
                 for (int kb = 0; kb < nkt; ++kb, ++it) {
                     const int s = it % TC_STAGES;
@@ -224,7 +239,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(a * TC_BN);
-                const int m0 = (t % tiles_m) * TC_BM;
+                int tm, tn;
+                tile_of(t, tm, tn);
+                const int m0 = tm * TC_BM;
                 const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
                 bool ok = true;
                 for (int kb = 0; kb < nkt; ++kb, ++it) {
@@ -265,7 +282,9 @@ __global__ void __launch_bounds__(192, 1)
         int i = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int a = i & 1;
-            const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * TC_BN;
+            int tm, tn;
+            tile_of(t, tm, tn);
+            const int m0 = tm * TC_BM, n0 = tn * TC_BN;
             const int64_t gr = m0 + 32 * quarter + lane;
             const bool row_ok = gr < g.M;
             float cnext[32];
