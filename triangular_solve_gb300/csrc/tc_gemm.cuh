@@ -160,12 +160,19 @@ __global__ void __launch_bounds__(192, 1)
     // column tiles together, so a wave of CTAs shares a few A tiles and a few
     // X tiles in L2 instead of streaming the whole A panel once per column
     // tile (the operand panels of large solves exceed L2).
+    // Triangular A (the block apply): the row tiles' K extents grow with the
+    // row, and with one group of row tiles a CTA would meet the same row tile
+    // in every round; reversing the row order on odd rounds pairs heavy with
+    // light tiles.  Only when each round holds whole column groups (then the
+    // mapping stays one-to-one).
+    const bool flip = g.a_lower && tiles_m <= kTileGroup && (int)gridDim.x % tiles_m == 0;
     auto tile_of = [&](int t, int &tm, int &tn) {
         const int per = kTileGroup * tiles_n;
         const int grp = t / per, rem = t - grp * per;
         const int gsize = min(kTileGroup, tiles_m - grp * kTileGroup);
         tm = grp * kTileGroup + rem % gsize;
         tn = rem / gsize;
+        if (flip && ((t / (int)gridDim.x) & 1)) tm = tiles_m - 1 - tm;
     };
     const int ntiles = tiles_m * (int)((g.N + TC_BN - 1) / TC_BN);
 
