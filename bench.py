@@ -425,6 +425,23 @@ def run_large(torch, tg, dev, stream, peaks, reps=2):
     return res
 
 
+def pipe_peaks():
+    """TFLOP/s of dependent-free FMA loops on every SM: FP32 FMA, paired FP32
+    FMA, FP64 FMA and the FP64 warp MMA (m8n8k4), three measurements each."""
+    import ctypes
+
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    lib = ctypes.CDLL(tgb.PROBE_LIB)
+    lib.trsm_probe_pipe_tflops.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.trsm_probe_pipe_tflops.restype = ctypes.c_double
+    out = {}
+    for kind, name in ((0, "ffma"), (3, "ffma2"), (1, "dfma"), (2, "dmma")):
+        out[name] = [round(lib.trsm_probe_pipe_tflops(kind, 10), 3) for _ in range(3)]
+    print(json.dumps({"pipe_tflops": out}), flush=True)
+    return out
+
+
 def nb_sweep(args):
     import torch
 
@@ -576,6 +593,8 @@ def main():
     ap.add_argument("--nb-sweep", action="store_true")
     ap.add_argument("--sweep-dtypes", default="f32,f64,c64,c128")
     ap.add_argument("--sweep-ms", default="1024,2048,4096,8192,16384")
+    ap.add_argument("--pipe-peaks", action="store_true",
+                    help="measure the FFMA / paired-FFMA / DFMA / DMMA pipe rates (csrc/probe/pipe_peaks.cu)")
     ap.add_argument("--sweep-reps", type=int, default=3)
     ap.add_argument("--sweep-nbs", default="128,256,512", help="block sizes of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -592,6 +611,9 @@ def main():
         return
     if args.nb_sweep:
         nb_sweep(args)
+        return
+    if args.pipe_peaks:
+        pipe_peaks()
         return
     run_gb300(args, ws, rank, local)
 
