@@ -116,3 +116,33 @@ def test_cpu_tensors_are_refused():
     B = torch.ones(4, 2, dtype=torch.float64)
     with pytest.raises(ValueError):
         tg.solve(A, B)
+
+
+def test_host_entry_argument_errors_and_quick_returns(lib):
+    """trsm_llnn_strided_batched_host validates like the device entry point
+    and returns before touching any memory or device on quick returns."""
+    one = ctypes.byref(ctypes.c_float(1.0))
+    fake = 1 << 20  # never dereferenced
+    f = lib.trsm_llnn_strided_batched_host
+    assert f(9, 0, 4, 4, one, fake, 4, 16, fake, 4, 16, 2, None) == -1
+    assert f(0, 2, 4, 4, one, fake, 4, 16, fake, 4, 16, 2, None) == -2
+    assert f(0, 0, -1, 4, one, fake, 4, 16, fake, 4, 16, 2, None) == -3
+    assert f(0, 0, 4, -1, one, fake, 4, 16, fake, 4, 16, 2, None) == -4
+    assert f(0, 0, 4, 4, None, fake, 4, 16, fake, 4, 16, 2, None) == -5
+    assert f(0, 0, 4, 4, one, None, 4, 16, fake, 4, 16, 2, None) == -6
+    assert f(0, 0, 4, 4, one, fake, 3, 16, fake, 4, 16, 2, None) == -7
+    assert f(0, 0, 4, 4, one, fake, 4, -1, fake, 4, 16, 2, None) == -8
+    assert f(0, 0, 4, 4, one, fake, 4, 16, None, 4, 16, 2, None) == -9
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 3, 16, 2, None) == -10
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 4, 15, 2, None) == -11
+    assert f(0, 0, 4, 4, one, fake, 4, 16, fake, 4, 16, -1, None) == -12
+    assert f(0, 0, 0, 4, one, None, 1, 0, None, 1, 4, 2, None) == 0
+    assert f(0, 0, 4, 0, one, None, 4, 0, None, 4, 0, 2, None) == 0
+    assert f(0, 0, 4, 4, one, None, 4, 16, None, 4, 16, 0, None) == 0
+
+
+def test_small_regime_rejects_too_many_columns(lib):
+    one = ctypes.byref(ctypes.c_double(1.0))
+    fake = 1 << 20
+    n = 64 * 65535 + 1  # beyond the small kernels' column grid
+    assert lib.trsm_llnn(1, 64, n, one, fake, 64, fake, 64, None) == -3
