@@ -1,7 +1,7 @@
-// mbarrier and bulk-copy helpers shared by the kernels that move data with
-// the TMA engine or wait on tensor-core work.  Every wait is bounded: after kWaitLimit polls it gives
-// up and the caller records TRSM_ERR_DEVICE_TIMEOUT in the device status
-// word instead of hanging.
+// mbarrier and TMA tensor-copy helpers shared by the kernels that move data
+// with the TMA engine or wait on tensor-core work.  Every wait is bounded:
+// after kWaitLimit polls it gives up and the caller records
+// TRSM_ERR_DEVICE_TIMEOUT in the device status word instead of hanging.
 #pragma once
 
 #include <cuda.h>
@@ -49,15 +49,6 @@ __device__ __forceinline__ void record_timeout(int *status) {
     if (status) atomicExch(status, TRSM_ERR_DEVICE_TIMEOUT);
 }
 
-// One-dimensional bulk copy global -> shared (the TMA engine), completion
-// counted in bytes on `bar`.  Both addresses 16-byte aligned, bytes a
-// multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // Three-dimensional tiled tensor copies (coordinates innermost first): load
 // into shared memory with completion on `bar`, store from shared memory in
 // the thread's bulk group.
@@ -75,13 +66,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int 
                  : "memory");
 }
 
-// One-dimensional bulk copy shared -> global, tracked per thread in bulk
-// groups: commit, then wait until the source reads (or the whole copies)
-// of all but the newest N groups are done.
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
+// Bulk copies (the tensor stores above) are tracked per thread in bulk
+// groups: commit, then wait until the source reads (or the whole copies) of
+// all but the newest N groups are done.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
