@@ -142,6 +142,16 @@ namespace {
 
 int split_rows(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, float *lo, int64_t ldd,
                cudaStream_t st) {
+    const bool v4 = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(hi) |
+                      reinterpret_cast<uintptr_t>(lo)) & 15) == 0 && ks % 4 == 0 && Kc % 4 == 0 && ldd % 4 == 0;
+    if (v4) {
+        const int64_t k4 = Kc / 4;
+        const dim3 grid((unsigned)((k4 + 127) / 128), (unsigned)(R < 65535 ? R : 65535));
+        split_rows_tf32_v4_kernel<<<grid, 128, 0, st>>>(reinterpret_cast<const float4 *>(src), ks / 4, R, k4,
+                                                        reinterpret_cast<float4 *>(hi), reinterpret_cast<float4 *>(lo),
+                                                        ldd / 4);
+        return launch_status();
+    }
     const dim3 grid((unsigned)((Kc + 127) / 128), (unsigned)(R < 65535 ? R : 65535));
     split_rows_tf32_kernel<<<grid, 128, 0, st>>>(src, ks, R, Kc, hi, lo, ldd);
     return launch_status();
