@@ -97,7 +97,7 @@ def test_inverse_blocks_times_diagonal_blocks_is_identity(env):
         assert np.all(np.triu(Wt, 1) == 0)
 
 
-@pytest.mark.parametrize("dtype", ["f64", "c128"])
+@pytest.mark.parametrize("dtype", ["f64", "c128", "f32"])
 def test_profile_reports_the_three_phases(env, dtype):
     torch, tg = env["torch"], env["tg"]
     m = n = 1024
@@ -150,6 +150,23 @@ def test_tensor_core_products_ragged(env, dtype, nb, m, n):
     xg, xr = _ex_solve(env, dtype, L, B, alpha, nb, lda=m + 4, ldb=m + 8)
     assert env["tg"].trsm_device_status() == 0
     assert_parity(dtype, xg, xr, f"tc {dtype} m={m} n={n} nb={nb}")
+
+
+@pytest.mark.parametrize("m,n,nb,ld_pad", [
+    (512, 256, 256, 0),    # two blocks: one update, then both applies in one launch
+    (528, 257, 256, 1),    # 16-row last block, one column past a tile, odd ldb (scalar splits)
+    (520, 300, 256, 0),    # 8-row last block: the per-block flow
+    (1280, 600, 128, 3),   # ten blocks, ragged column tiles
+    (3000, 512, 512, 0),   # 440-row last block
+])
+def test_lookahead_flow_edges(env, m, n, nb, ld_pad):
+    """f32 look-ahead form (update t, the scaled panel L_panel D^-1 of block
+    t+1 and the apply of block t-1 in one launch): block counts, last-block
+    sizes, column raggedness and leading dimensions at its edges."""
+    L, B = ti.generate("f32", m, n, 1, kind="ddm", seed=m + n + nb)
+    xg, xr = _ex_solve(env, "f32", L, B, -0.75, nb, lda=m + ld_pad, ldb=m + ld_pad)
+    assert env["tg"].trsm_device_status() == 0
+    assert_parity("f32", xg, xr, f"look-ahead m={m} n={n} nb={nb}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "c64"])

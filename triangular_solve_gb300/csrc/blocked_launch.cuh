@@ -222,6 +222,24 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     reinterpret_cast<typename Elem<T>::Real *>(&minus_one)[0] = -1;
 
     const int64_t tb = (m + nb - 1) / nb;
+    if constexpr (std::is_same<T, float>::value) {
+        if (tc_panels && tc_fused_usable(m, n, nb)) {
+            // look-ahead form (tc_gemm.cu): every launch but the last is an
+            // update with the previous block's apply folded in (phase 2);
+            // the last holds the two remaining applies (phase 1)
+            timer.begin();
+            rc = tc_fused_prepare(m, n, nb, L, a.lda, W, tc_panels, st);
+            for (int64_t t = 0; !rc && t + 1 < tb; ++t)
+                rc = tc_fused_step(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            if (rc || (rc = timer.end(2))) return rc;
+            timer.begin();
+            rc = tc_fused_step(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            if (rc || (rc = timer.end(1))) return rc;
+            if (a.ms)
+                for (int q = 0; q < 3; ++q) a.ms[q] = timer.acc[q];
+            return TRSM_SUCCESS;
+        }
+    }
     for (int64_t t = 0; t < tb; ++t) {
         const int64_t r0 = t * nb;
         const int64_t mb = (m - r0 < nb) ? m - r0 : nb;

@@ -67,7 +67,9 @@ inline int64_t panel_ld(int64_t n) { return ((n > 0 ? n : 1) + 3) / 4 * 4; }
 inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 // f32 adds the TF32 head/tail panels of the tensor-core products
 // (tc_panel_bytes: the A operand -- L panel or D_t^-1 --, the X operand and
-// the split X_t the apply leaves for the update, two copies each, K-major).
+// the split X_t the apply leaves for the update, two copies each, K-major;
+// or, when the look-ahead form applies and needs more, its panels:
+// tc_fused_bytes).
 // c64 adds the real-form operands of its tensor-core products
 // (tc_panel_bytes_c64: A' = m x 2nb, X' = 2n x 2nb and the split X_t' the
 // apply leaves for the update, two copies each).
@@ -96,6 +98,14 @@ int tc_update_c64(int64_t M, int64_t N, int64_t K, const float2 *A, int64_t lda,
                   float2 *C, int64_t ldc, float2 beta, int64_t Mmax, void *panels, cudaStream_t st);
 int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, int64_t ldb, float gamma,
                  int64_t Mmax, void *panels, bool emit_split, cudaStream_t st);
+// Look-ahead form of the f32 solve on the tensor cores (tc_gemm.cu): after
+// the inversion, tc_fused_prepare once, then tc_fused_step for t = 0 .. tb-1.
+bool tc_fused_usable(int64_t m, int64_t n, int64_t nb);
+size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb);
+int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, void *panels,
+                     cudaStream_t st);
+int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
+                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st);
 // Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).
 int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
                    const uint32_t *box, bool swizzle128);

@@ -123,7 +123,9 @@ static TcPanels tc_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
 }
 
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb) {
-    return (size_t)(2 * round256(m * nb * 4) + 4 * round256(n * nb * 4));
+    const size_t per_block = (size_t)(2 * round256(m * nb * 4) + 4 * round256(n * nb * 4));
+    const size_t fused = tc_fused_usable(m, n, nb) ? tc_fused_bytes(m, n, nb) : 0;
+    return per_block > fused ? per_block : fused;
 }
 
 bool tc_update_usable(int64_t M, int64_t N, int64_t K) {
@@ -157,28 +159,64 @@ int split_rows(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, f
     return launch_status();
 }
 
-int launch_tc(const float *a_hi, const float *a_lo, const float *x_hi, const float *x_lo, TcArgs g, cudaStream_t st) {
-    CUtensorMap ma_hi, ma_lo, mx_hi, mx_lo;
+int sm_count() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 152;
+    }
+    return sms;
+}
+
+// Problem q of a launch: tensor maps over the K-major head/tail buffers of A
+// (a_rows rows) and X (x_rows rows), row stride ld floats, K extent g.K (the
+// loads zero-fill past it).  Row extents may exceed g.M / g.N (padded
+// buffers): rows past them only feed outputs the epilogue discards.
+int tc_problem(TcProblem &q, const float *a_hi, const float *a_lo, int64_t a_rows, const float *x_hi,
+               const float *x_lo, int64_t x_rows, int64_t ld, const TcArgs &g) {
     int rc;
-    if ((rc = make_map(&ma_hi, a_hi, g.M, g.K, g.K, TC_BM))) return rc;
-    if ((rc = make_map(&ma_lo, a_lo, g.M, g.K, g.K, TC_BM))) return rc;
-    if ((rc = make_map(&mx_hi, x_hi, g.N, g.K, g.K, TC_BN))) return rc;
-    if ((rc = make_map(&mx_lo, x_lo, g.N, g.K, g.K, TC_BN))) return rc;
-    if ((rc = device_status_word(&g.status))) return rc;
+    if ((rc = make_map(&q.a_hi, a_hi, a_rows, g.K, ld, TC_BM))) return rc;
+    if ((rc = make_map(&q.a_lo, a_lo, a_rows, g.K, ld, TC_BM))) return rc;
+    if ((rc = make_map(&q.x_hi, x_hi, x_rows, g.K, ld, TC_BN))) return rc;
+    if ((rc = make_map(&q.x_lo, x_lo, x_rows, g.K, ld, TC_BN))) return rc;
+    q.g = g;
+    q.tiles_m = (int)((g.M + TC_BM - 1) / TC_BM);
+    q.tiles_n = (int)((g.N + TC_BN - 1) / TC_BN);
+    q.nk = (int)((g.K + TC_BK - 1) / TC_BK);
+    return TRSM_SUCCESS;
+}
+
+static_assert(sizeof(TcLaunch) <= 4096, "kernel parameters");
+
+// One persistent launch over the tiles of P.p[0 .. np-1].
+int tc_launch(TcLaunch &P, int np, cudaStream_t st) {
+    int rc;
+    if ((rc = device_status_word(&P.status))) return rc;
+    P.np = np;
+    int64_t tiles = 0;
+    for (int i = 0; i < np; ++i) {
+        P.p[i].tile_begin = (int)tiles;
+        tiles += (int64_t)P.p[i].tiles_m * P.p[i].tiles_n;
+    }
+    if (tiles == 0) return TRSM_SUCCESS;
+    if (tiles > INT32_MAX) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
+    P.ntiles = (int)tiles;
     const cudaError_t e =
         cudaFuncSetAttribute(tc_update_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return cuda_status(e);
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 152;
-    }
-    const int64_t tiles = ((g.M + TC_BM - 1) / TC_BM) * ((g.N + TC_BN - 1) / TC_BN);
+    const int sms = sm_count();
     const unsigned ctas = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
-    tc_update_f32_kernel<<<ctas, 192, TC_SMEM, st>>>(ma_hi, ma_lo, mx_hi, mx_lo, g);
+    tc_update_f32_kernel<<<ctas, 192, TC_SMEM, st>>>(P);
     return launch_status();
+}
+
+int launch_tc(const float *a_hi, const float *a_lo, const float *x_hi, const float *x_lo, const TcArgs &g,
+              cudaStream_t st) {
+    TcLaunch P;
+    const int rc = tc_problem(P.p[0], a_hi, a_lo, g.M, x_hi, x_lo, g.N, g.K, g);
+    return rc ? rc : tc_launch(P, 1, st);
 }
 
 TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
@@ -194,10 +232,10 @@ TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
     g.gamma_im = 0.f;
     g.beta_zero = 0;
     g.a_lower = 0;
+    g.a_upper = 0;
     g.cplx = 0;
     g.xhi = g.xlo = nullptr;
     g.ldxs = 0;
-    g.status = nullptr;
     return g;
 }
 
@@ -327,6 +365,155 @@ int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, 
         g.ldxs = nb;
     }
     return launch_tc(p.a_hi, p.a_lo, p.x_hi, p.x_lo, g, st);
+}
+
+// ---------------------------------------------------------------------------
+// Look-ahead form of the f32 blocked solve.  With W_t = L_panel_t D_t^-1
+// (L_panel_t: the rows of L below block t, in its columns) the update of
+// block t reads the block row R_t itself,
+//     B_below -= W_t R_t,
+// so X_t = D_t^-1 R_t is off the path from one block to the next.  Launch t
+// computes, as one tile list:
+//   the update of block t      (m - r0 - nb) x n x nb,
+//   W_{t+1} for the next step  (W_{t+1}^T = D_{t+1}^-T L_panel_{t+1}^T,
+//                              nb x (m - r1 - nb) x nb, upper-triangular A,
+//                              stored split: the A operand of update t+1),
+//   the apply of block t-1     nb x n x nb, lower-triangular A, over R_{t-1},
+// and the last launch both remaining applies.  The apply thus fills the
+// rounds of the update instead of running in under two rounds of its own,
+// and no split copy of X_t is written.  W_0 is computed before the first
+// step.  Extra work: the W_t products, nb/n of the updates' flops (half of it
+// with the triangular K range).
+//
+// Workspace (256-byte aligned regions, rows padded for the TMA boxes):
+//   wp[2]   W_t head/tail, RA x nb (A operand of the update; double buffer)
+//   lp      L_panel_{t+1} head/tail, RA x nb (X operand of W_{t+1}^T)
+//   xs[2]   R_t head/tail, RX x nb (X operand of update t and apply t)
+//   d0, d1  D^-1 (apply) or D^-T (W product) rows, head/tail, nb x nb
+// with RA = m and RX = n rounded up to 256 rows.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Below this many right-hand sides the W_t products (nb/n of the update
+// flops) and the narrow tiles make the per-block flow the faster one.
+constexpr int64_t kTcFusedMinN = 256;
+
+struct TcFused {
+    float *wp_hi[2], *wp_lo[2], *lp_hi, *lp_lo, *xs_hi[2], *xs_lo[2], *d0_hi, *d0_lo, *d1_hi, *d1_lo;
+    int64_t ra, rx;
+};
+
+int64_t round_rows(int64_t r) { return (r + 255) / 256 * 256; }
+
+TcFused tc_fused_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
+    TcFused f;
+    f.ra = round_rows(m);
+    f.rx = round_rows(n);
+    const size_t A = round256(f.ra * nb * 4), X = round256(f.rx * nb * 4), D = round256(nb * nb * 4);
+    char *c = static_cast<char *>(panels);
+    auto take = [&](size_t bytes) {
+        float *p = reinterpret_cast<float *>(c);
+        c += bytes;
+        return p;
+    };
+    for (int i = 0; i < 2; ++i) {
+        f.wp_hi[i] = take(A);
+        f.wp_lo[i] = take(A);
+    }
+    f.lp_hi = take(A);
+    f.lp_lo = take(A);
+    for (int i = 0; i < 2; ++i) {
+        f.xs_hi[i] = take(X);
+        f.xs_lo[i] = take(X);
+    }
+    f.d0_hi = take(D);
+    f.d0_lo = take(D);
+    f.d1_hi = take(D);
+    f.d1_lo = take(D);
+    return f;
+}
+
+// The W_{t+1}^T product of launch t (and of the preparation, t = -1): block
+// b = t + 1, its L panel and D_b^-T split, then the problem emitting W_b.
+int tc_w_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t nb, const float *L, int64_t lda,
+                 const float *W, cudaStream_t st) {
+    const int64_t r1 = b * nb, rows = m - r1 - nb;
+    int rc = split(L + r1 * lda + r1 + nb, lda, rows, nb, f.lp_hi, f.lp_lo, nb, st);  // L panel rows, K-major
+    if (!rc) rc = split_rows(W + b * nb * nb, nb, nb, nb, f.d1_hi, f.d1_lo, nb, st);  // rows of D_b^-T
+    if (rc) return rc;
+    TcArgs g = tc_args(nb, rows, nb, nullptr, 0);
+    g.beta_zero = 1;
+    g.gamma = 1.f;
+    g.a_upper = 1;
+    g.xhi = f.wp_hi[b & 1];
+    g.xlo = f.wp_lo[b & 1];
+    g.ldxs = nb;
+    return tc_problem(q, f.d1_hi, f.d1_lo, nb, f.lp_hi, f.lp_lo, f.ra, nb, g);
+}
+
+// The apply of block b over its block row (R_b split in xs[b & 1]); the D_b^-1
+// rows go to (dh, dl).
+int tc_x_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t n, int64_t nb, const float *W,
+                 float *B, int64_t ldb, float gamma, float *dh, float *dl, cudaStream_t st) {
+    const int64_t r0 = b * nb, mb = (m - r0 < nb) ? m - r0 : nb;
+    const int rc = split(W + b * nb * nb, nb, mb, mb, dh, dl, nb, st);  // rows of D_b^-1, K-major
+    if (rc) return rc;
+    TcArgs g = tc_args(mb, n, mb, B + r0, ldb);
+    g.beta_zero = 1;
+    g.gamma = gamma;
+    g.a_lower = 1;
+    return tc_problem(q, dh, dl, nb, f.xs_hi[b & 1], f.xs_lo[b & 1], f.rx, nb, g);
+}
+
+}  // namespace
+
+bool tc_fused_usable(int64_t m, int64_t n, int64_t nb) {
+    if (nb != 128 && nb != 256 && nb != 512) return false;
+    const int64_t tb = (m + nb - 1) / nb, mb_last = m - (tb - 1) * nb;
+    const int64_t tiles = ((m + TC_BM - 1) / TC_BM) * ((n + TC_BN - 1) / TC_BN);
+    return tb >= 2 && mb_last >= TC_BK && n >= kTcFusedMinN && tiles < INT32_MAX;
+}
+
+size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb) {
+    const int64_t ra = round_rows(m), rx = round_rows(n);
+    return (size_t)(6 * round256(ra * nb * 4) + 4 * round256(rx * nb * 4) + 4 * round256(nb * nb * 4));
+}
+
+// W_0 = L_panel_0 D_0^-1, before step 0.
+int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, void *panels,
+                     cudaStream_t st) {
+    const TcFused f = tc_fused_layout(panels, m, n, nb);
+    TcLaunch P;
+    const int rc = tc_w_problem(P.p[0], f, 0, m, nb, L, lda, W, st);
+    return rc ? rc : tc_launch(P, 1, st);
+}
+
+// Step t: split R_t, then one launch of update t, W_{t+1} and apply t-1 (the
+// last step: apply t and apply t-1).  alpha enters through block 0.
+int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
+                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st) {
+    const TcFused f = tc_fused_layout(panels, m, n, nb);
+    const int64_t tb = (m + nb - 1) / nb, r0 = t * nb, mb = (m - r0 < nb) ? m - r0 : nb;
+    int rc = split_rows(B + r0, ldb, n, mb, f.xs_hi[t & 1], f.xs_lo[t & 1], nb, st);  // columns of R_t
+    if (rc) return rc;
+    TcLaunch P;
+    int np = 0;
+    if (t + 1 < tb) {
+        TcArgs g = tc_args(m - r0 - nb, n, nb, B + r0 + nb, ldb);
+        g.beta = t == 0 ? alpha : 1.f;
+        g.gamma = t == 0 ? -alpha : -1.f;
+        if ((rc = tc_problem(P.p[np++], f.wp_hi[t & 1], f.wp_lo[t & 1], f.ra, f.xs_hi[t & 1], f.xs_lo[t & 1], f.rx,
+                             nb, g)))
+            return rc;
+        if (r0 + 2 * nb < m && (rc = tc_w_problem(P.p[np++], f, t + 1, m, nb, L, lda, W, st))) return rc;
+    } else if ((rc = tc_x_problem(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : 1.f, f.d1_hi, f.d1_lo,
+                                  st))) {
+        return rc;
+    }
+    if (t >= 1 &&
+        (rc = tc_x_problem(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : 1.f, f.d0_hi, f.d0_lo, st)))
+        return rc;
+    return tc_launch(P, np, st);
 }
 
 int device_status(int clear) {

@@ -1,18 +1,20 @@
-// Trailing-update GEMM for f32 on the fifth-generation tensor cores
-// (tcgen05, sm_100 family):  C = beta*C - A * X
-// with A (M x K) the L panel and X (K x N) the X_t panel, K = NB.
+// f32 products of the blocked solve on the fifth-generation tensor cores
+// (tcgen05, sm_100 family):  C = beta*C + gamma * A X
+// with A (M x K) and X (K x N) stored K-major: the trailing update (A the
+// L panel or L_panel D_t^-1, X the block row), the block apply (A = D_t^-1,
+// lower triangular) and the scaled panel (L_panel D_t^-1)^T (A = D_t^-T,
+// upper triangular).
 //
 // f32 accuracy from TF32 tensor cores: each operand is split into a TF32
 // head and a TF32 tail (a = hi + lo, hi = tf32(a), lo = tf32(a - hi)) by a
 // preprocessing pass, and the product is accumulated in FP32 as
 //     A_hi X_hi + A_hi X_lo + A_lo X_hi
-// (the dropped A_lo X_lo term is ~2^-22 relative).  The operands are stored
-// K-major (row-major panels), the layout the tensor-core descriptors read.
+// (the dropped A_lo X_lo term is ~2^-22 relative).
 //
 // Persistent kernel, one CTA per SM, each CTA taking 128 x 256 output tiles
-// in turn, with six warps:
+// in turn (of up to three independent products per launch), with six warps:
 //   warp 0  TMA producer: 2-D tensor loads of the four operand tiles of a
-//           32-deep K slab into a two-stage shared-memory ring (128-byte
+//           16-deep K slab into a four-stage shared-memory ring (64-byte
 //           swizzle), completion counted on the stage's "full" mbarrier;
 //           the ring runs on from one tile to the next;
 //   warp 1  MMA issuer: one elected thread issues tcgen05.mma (kind::tf32,
@@ -20,7 +22,7 @@
 //           tensor memory (2 x 256 columns); tcgen05.commit frees each stage
 //           and signals "accumulator full";
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, release of the
-//           accumulator, then C = beta*C - acc straight to global memory
+//           accumulator, then the output straight to global memory
 //           (coalesced per column) while the MMAs of the next tile run.
 // Every mbarrier wait is bounded: when a wait expires the kernel records
 // TRSM_ERR_DEVICE_TIMEOUT in a device status word and the CTA unwinds
@@ -63,14 +65,33 @@ constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYT
 // gamma = gamma + i*gamma_im multiply complex values; with xhi set the
 // split copy is the X' operand of tc_update_c64: row 2j = [Re | -Im],
 // row 2j+1 = [Im | Re], halves ldxs/2 apart.
+// a_upper: A is upper triangular, a row tile starts its K loop at its first
+// row.  C == nullptr (with beta_zero and xhi set): only the split copy is
+// stored.
 struct TcArgs {
     int64_t M, N, K;
     float *C;
     int64_t ldc;
     float beta, beta_im, gamma, gamma_im;
-    int beta_zero, a_lower, cplx;
+    int beta_zero, a_lower, a_upper, cplx;
     float *xhi, *xlo;
     int64_t ldxs;
+};
+
+// One launch computes up to kTcMaxProblems independent products: their tiles
+// are numbered one problem after the other (problem i owns tiles
+// tile_begin .. tile_begin + tiles_m * tiles_n - 1), and the persistent CTAs
+// walk the concatenated list, so a small or triangular product fills the
+// rounds of a larger one instead of running a partly idle launch of its own.
+constexpr int kTcMaxProblems = 3;
+struct TcProblem {
+    CUtensorMap a_hi, a_lo, x_hi, x_lo;  // K-major operand tiles, head and tail
+    TcArgs g;
+    int tile_begin, tiles_m, tiles_n, nk;
+};
+struct TcLaunch {
+    TcProblem p[kTcMaxProblems];
+    int np, ntiles;
     int *status;  // device status word (0 = ok)
 };
 
@@ -134,10 +155,7 @@ __device__ __forceinline__ float to_tf32(float x) {
 // on across tile boundaries, and the accumulator alternates between two
 // 256-column halves of tensor memory: the MMA warp fills one while the
 // epilogue warps drain the other (acc_full / acc_empty barriers).
-__global__ void __launch_bounds__(192, 1)
-    tc_update_f32_kernel(const __grid_constant__ CUtensorMap mA_hi, const __grid_constant__ CUtensorMap mA_lo,
-                         const __grid_constant__ CUtensorMap mX_hi, const __grid_constant__ CUtensorMap mX_lo,
-                         const TcArgs g) {
+__global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_constant__ TcLaunch P) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment for the swizzled tiles
@@ -151,31 +169,50 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t drain = bars + 8u * (2 * TC_STAGES + 4);  // last commit of the MMA thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + kTmemSlotOffset);
     __shared__ int abort_flag;
+    // the problems' arguments and tile counts, staged once: the tile loops
+    // index them by problem, and a dynamically indexed kernel parameter is a
+    // generic load on every use
+    __shared__ TcArgs s_args[kTcMaxProblems];
+    __shared__ int4 s_tiles[kTcMaxProblems];  // tile_begin, tiles_m, tiles_n, nk
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = (int)((g.K + TC_BK - 1) / TC_BK);
-    const int tiles_m = (int)((g.M + TC_BM - 1) / TC_BM);
-    const int tiles_n = (int)((g.N + TC_BN - 1) / TC_BN);
-    // Tile t -> (row tile, column tile), grouped: kTileGroup row tiles walk all
-    // column tiles together, so a wave of CTAs shares a few A tiles and a few
-    // X tiles in L2 instead of streaming the whole A panel once per column
-    // tile (the operand panels of large solves exceed L2).
-    // Triangular A (the block apply): the row tiles' K extents grow with the
-    // row, and with one group of row tiles a CTA would meet the same row tile
-    // in every round; reversing the row order on odd rounds pairs heavy with
-    // light tiles.  Only when each round holds whole column groups (then the
-    // mapping stays one-to-one).
-    const bool flip = g.a_lower && tiles_m <= kTileGroup && (int)gridDim.x % tiles_m == 0;
-    auto tile_of = [&](int t, int &tm, int &tn) {
-        const int per = kTileGroup * tiles_n;
-        const int grp = t / per, rem = t - grp * per;
-        const int gsize = min(kTileGroup, tiles_m - grp * kTileGroup);
+    const int ntiles = P.ntiles, np = P.np;
+    // Tile t -> (problem, row tile, column tile).  Within a problem the order
+    // is grouped: kTileGroup row tiles walk all column tiles together, so a
+    // wave of CTAs shares a few A tiles and a few X tiles in L2 instead of
+    // streaming the whole A panel once per column tile (the operand panels of
+    // large solves exceed L2).
+    // Triangular A alone in a launch (the block apply): the row tiles' K
+    // extents grow with the row, and with one group of row tiles a CTA would
+    // meet the same row tile in every round; reversing the row order on odd
+    // rounds pairs heavy with light tiles.  Only when each round holds whole
+    // column groups (then the mapping stays one-to-one).
+    auto tile_of = [&](int t, int &pq, int &tm, int &tn) {
+        pq = 0;
+        while (pq + 1 < np && t >= s_tiles[pq + 1].x) ++pq;
+        const int4 q = s_tiles[pq];
+        const int u = t - q.x;
+        const int per = kTileGroup * q.z;
+        const int grp = u / per, rem = u - grp * per;
+        const int gsize = min(kTileGroup, q.y - grp * kTileGroup);
         tm = grp * kTileGroup + rem % gsize;
         tn = rem / gsize;
-        if (flip && ((t / (int)gridDim.x) & 1)) tm = tiles_m - 1 - tm;
+        const bool flip = np == 1 && s_args[0].a_lower && q.y <= kTileGroup && (int)gridDim.x % q.y == 0;
+        if (flip && ((t / (int)gridDim.x) & 1)) tm = q.y - 1 - tm;
     };
-    const int ntiles = tiles_m * (int)((g.N + TC_BN - 1) / TC_BN);
+    // K slabs [kb0, kb1) of row tile m0 of problem pq: a triangular A has
+    // zeros past (lower) or before (upper) the tile's rows
+    auto k_range = [&](int pq, int m0, int &kb0, int &kb1) {
+        const int nk = s_tiles[pq].w, lower = s_args[pq].a_lower;
+        kb0 = s_args[pq].a_upper ? m0 / TC_BK : 0;
+        kb1 = lower ? min(nk, lower * (m0 + TC_BM) / TC_BK) : nk;
+    };
 
+    if (threadIdx.x < np) {
+        const TcProblem &q = P.p[threadIdx.x];
+        s_args[threadIdx.x] = q.g;
+        s_tiles[threadIdx.x] = make_int4(q.tile_begin, q.tiles_m, q.tiles_n, q.nk);
+    }
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < TC_STAGES; ++s) {
@@ -201,7 +238,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
     auto aborted = [&]() { return *(volatile int *)&abort_flag != 0; };
     auto fail = [&]() {
-        record_timeout(g.status);
+        record_timeout(P.status);
         abort_flag = 1;
     };
 
@@ -209,11 +246,13 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
-                int tm, tn;
-                tile_of(t, tm, tn);
+                int pq, tm, tn;
+                tile_of(t, pq, tm, tn);
+                const TcProblem &q = P.p[pq];
                 const int m0 = tm * TC_BM, n0 = tn * TC_BN;
-                const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
-                for (int kb = 0; kb < nkt; ++kb, ++it) {
+                int kb0, kb1;
+                k_range(pq, m0, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % TC_STAGES;
                     if (it >= TC_STAGES && !mbar_wait(empty(s), ((it / TC_STAGES) - 1) & 1)) {
                         fail();
@@ -222,16 +261,16 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t st = base + s * TC_STAGE_BYTES;
                     mbar_expect_tx(full(s), TC_STAGE_BYTES);
                     const int kx = kb * TC_BK;
-                    tma_load_2d(st, &mA_hi, kx, m0, full(s));
-                    tma_load_2d(st + TC_A_BYTES, &mA_lo, kx, m0, full(s));
-                    tma_load_2d(st + 2 * TC_A_BYTES, &mX_hi, kx, n0, full(s));
-                    tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &mX_lo, kx, n0, full(s));
+                    tma_load_2d(st, &q.a_hi, kx, m0, full(s));
+                    tma_load_2d(st + TC_A_BYTES, &q.a_lo, kx, m0, full(s));
+                    tma_load_2d(st + 2 * TC_A_BYTES, &q.x_hi, kx, n0, full(s));
+                    tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &q.x_lo, kx, n0, full(s));
                 }
             }
             if (aborted()) {
                 // loads nobody consumed must land before the CTA's shared memory goes away
                 for (int j = (it > TC_STAGES ? it - TC_STAGES : 0); j < it; ++j)
-                    if (!mbar_wait(full(j % TC_STAGES), (j / TC_STAGES) & 1)) record_timeout(g.status);
+                    if (!mbar_wait(full(j % TC_STAGES), (j / TC_STAGES) & 1)) record_timeout(P.status);
             }
         }
     } else if (warp == 1) {
@@ -246,12 +285,12 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(a * TC_BN);
-                int tm, tn;
-                tile_of(t, tm, tn);
-                const int m0 = tm * TC_BM;
-                const int nkt = g.a_lower ? min(nk, g.a_lower * (m0 + TC_BM) / TC_BK) : nk;
+                int pq, tm, tn;
+                tile_of(t, pq, tm, tn);
+                int kb0, kb1;
+                k_range(pq, tm * TC_BM, kb0, kb1);
                 bool ok = true;
-                for (int kb = 0; kb < nkt; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % TC_STAGES;
                     if (!mbar_wait(full(s), (it / TC_STAGES) & 1)) {
                         fail();
@@ -266,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
                         const uint64_t a_lo = tile_desc(st + TC_A_BYTES + kk * 32);
                         const uint64_t x_hi = tile_desc(st + 2 * TC_A_BYTES + kk * 32);
                         const uint64_t x_lo = tile_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
-                        mma_tf32(d, a_hi, x_hi, idesc, (kb | kk) != 0);
+                        mma_tf32(d, a_hi, x_hi, idesc, kb != kb0 || kk != 0);
                         mma_tf32(d, a_hi, x_lo, idesc, 1);
                         mma_tf32(d, a_lo, x_hi, idesc, 1);
                     }
@@ -277,7 +316,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             // every MMA issued here has finished before tensor memory is released
             mma_commit(drain);
-            if (!mbar_wait(drain, 0)) record_timeout(g.status);
+            if (!mbar_wait(drain, 0)) record_timeout(P.status);
         }
     } else {
         // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31.  A thread owns
@@ -289,21 +328,37 @@ __global__ void __launch_bounds__(192, 1)
         int i = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int a = i & 1;
-            int tm, tn;
-            tile_of(t, tm, tn);
+            int pq, tm, tn;
+            tile_of(t, pq, tm, tn);
+            const TcArgs &g = s_args[pq];
             const int m0 = tm * TC_BM, n0 = tn * TC_BN;
             const int64_t gr = m0 + 32 * quarter + lane;
             const bool row_ok = gr < g.M;
+            // loop invariants of the tile, hoisted: the column loops below
+            // are unrolled, and a full column tile storing only C (the
+            // update) runs without per-element checks
+            float *const C = g.C;
+            const int64_t ldc = g.ldc, N = g.N;
+            const float beta = g.beta, gamma = g.gamma;
+            const bool cplx = g.cplx != 0, load_c = !g.beta_zero && row_ok;
+            const bool plain_full = !cplx && g.xhi == nullptr && n0 + TC_BN <= N;
             float cnext[32];
             // element (gr, gc) of C
             auto coff = [&](int64_t gc) -> int64_t {
-                return g.cplx ? (gc >> 1) * g.ldc + 2 * gr + (gc & 1) : gc * g.ldc + gr;
+                return cplx ? (gc >> 1) * ldc + 2 * gr + (gc & 1) : gc * ldc + gr;
             };
             auto fetch = [&](int chunk, float(&dst)[32]) {
+                const int64_t gc0 = n0 + chunk * 32;
+                if (!load_c) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t gc = n0 + chunk * 32 + j;
-                    dst[j] = (!g.beta_zero && row_ok && gc < g.N) ? g.C[coff(gc)] : 0.f;
+                    for (int j = 0; j < 32; ++j) dst[j] = 0.f;
+                } else if (plain_full) {
+                    const float *cp = C + gc0 * ldc + gr;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dst[j] = cp[j * ldc];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dst[j] = (gc0 + j < N) ? C[coff(gc0 + j)] : 0.f;
                 }
             };
             fetch(0, cnext);
@@ -338,18 +393,19 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acc_empty(a));
                 }
-                if (row_ok && g.cplx) {
+                if (row_ok && cplx) {
+                    const float beta_im = g.beta_im, gamma_im = g.gamma_im;
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         const int64_t gc = n0 + chunk * 32 + j;  // even: a (re, im) pair
-                        if (gc < g.N) {
+                        if (gc < N) {
                             const float cr = ccur[j], ci = ccur[j + 1];
                             const float pr = __uint_as_float(v[j]), pi = __uint_as_float(v[j + 1]);
-                            const float ar = fmaf(g.gamma, pr, -g.gamma_im * pi);
-                            const float ai = fmaf(g.gamma, pi, g.gamma_im * pr);
-                            const float orr = fmaf(g.beta, cr, fmaf(-g.beta_im, ci, ar));
-                            const float oi = fmaf(g.beta, ci, fmaf(g.beta_im, cr, ai));
-                            *reinterpret_cast<float2 *>(g.C + coff(gc)) = make_float2(orr, oi);
+                            const float ar = fmaf(gamma, pr, -gamma_im * pi);
+                            const float ai = fmaf(gamma, pi, gamma_im * pr);
+                            const float orr = fmaf(beta, cr, fmaf(-beta_im, ci, ar));
+                            const float oi = fmaf(beta, ci, fmaf(beta_im, cr, ai));
+                            *reinterpret_cast<float2 *>(C + coff(gc)) = make_float2(orr, oi);
                             if (g.xhi) {
                                 const int64_t re_row = gc * g.ldxs, im_row = re_row + g.ldxs, half = g.ldxs / 2;
                                 auto put = [&](int64_t o, float x) {
@@ -364,17 +420,23 @@ __global__ void __launch_bounds__(192, 1)
                             }
                         }
                     }
+                } else if (row_ok && plain_full) {
+                    float *cp = C + (n0 + chunk * 32) * ldc + gr;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) cp[j * ldc] = fmaf(beta, ccur[j], gamma * __uint_as_float(v[j]));
                 } else if (row_ok) {
+                    float *const xhi = g.xhi, *const xlo = g.xlo;
+                    const int64_t ldxs = g.ldxs;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int64_t gc = n0 + chunk * 32 + j;
-                        if (gc < g.N) {
-                            const float o = fmaf(g.beta, ccur[j], g.gamma * __uint_as_float(v[j]));
-                            g.C[gc * g.ldc + gr] = o;
-                            if (g.xhi) {
+                        if (gc < N) {
+                            const float o = fmaf(beta, ccur[j], gamma * __uint_as_float(v[j]));
+                            if (C) C[gc * ldc + gr] = o;
+                            if (xhi) {
                                 const float h = to_tf32(o);
-                                g.xhi[gc * g.ldxs + gr] = h;
-                                g.xlo[gc * g.ldxs + gr] = to_tf32(o - h);
+                                xhi[gc * ldxs + gr] = h;
+                                xlo[gc * ldxs + gr] = to_tf32(o - h);
                             }
                         }
                     }
