@@ -228,7 +228,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
             // update with the previous block's apply folded in (phase 2);
             // the last holds the two remaining applies (phase 1)
             timer.begin();
-            rc = tc_fused_prepare(m, n, nb, L, a.lda, W, tc_panels, st);
+            rc = tc_fused_prepare(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st);
             for (int64_t t = 0; !rc && t + 1 < tb; ++t)
                 rc = tc_fused_step(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
             if (rc || (rc = timer.end(2))) return rc;

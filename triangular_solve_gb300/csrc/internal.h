@@ -102,8 +102,8 @@ int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, 
 // the inversion, tc_fused_prepare once, then tc_fused_step for t = 0 .. tb-1.
 bool tc_fused_usable(int64_t m, int64_t n, int64_t nb);
 size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb);
-int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, void *panels,
-                     cudaStream_t st);
+int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
+                     int64_t ldb, void *panels, cudaStream_t st);
 int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
                   float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st);
 // Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).

@@ -236,6 +236,7 @@ TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
     g.cplx = 0;
     g.xhi = g.xlo = nullptr;
     g.ldxs = 0;
+    g.xrows = M;
     return g;
 }
 
@@ -374,21 +375,24 @@ int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, 
 //     B_below -= W_t R_t,
 // so X_t = D_t^-1 R_t is off the path from one block to the next.  Launch t
 // computes, as one tile list:
-//   the update of block t      (m - r0 - nb) x n x nb,
+//   the update of block t      (m - r0 - nb) x n x nb, its first nb rows
+//                              (R_{t+1}, final now) also stored split: the
+//                              X operand of the next update and apply,
 //   W_{t+1} for the next step  (W_{t+1}^T = D_{t+1}^-T L_panel_{t+1}^T,
 //                              nb x (m - r1 - nb) x nb, upper-triangular A,
 //                              stored split: the A operand of update t+1),
 //   the apply of block t-1     nb x n x nb, lower-triangular A, over R_{t-1},
 // and the last launch both remaining applies.  The apply thus fills the
 // rounds of the update instead of running in under two rounds of its own,
-// and no split copy of X_t is written.  W_0 is computed before the first
-// step.  Extra work: the W_t products, nb/n of the updates' flops (half of it
+// no split copy of X_t is written, and no pass splits the block rows.  W_0
+// and the split of R_0 are made before the first step.  Extra work: the W_t products, nb/n of the updates' flops (half of it
 // with the triangular K range).
 //
 // Workspace (256-byte aligned regions, rows padded for the TMA boxes):
 //   wp[2]   W_t head/tail, RA x nb (A operand of the update; double buffer)
 //   lp      L_panel_{t+1} head/tail, RA x nb (X operand of W_{t+1}^T)
-//   xs[2]   R_t head/tail, RX x nb (X operand of update t and apply t)
+//   xs[3]   R_t head/tail, RX x nb (X operand of update t and apply t; launch
+//           t reads R_t and R_{t-1} and writes R_{t+1}: three buffers)
 //   d0, d1  D^-1 (apply) or D^-T (W product) rows, head/tail, nb x nb
 // with RA = m and RX = n rounded up to 256 rows.
 // ---------------------------------------------------------------------------
@@ -399,7 +403,7 @@ namespace {
 constexpr int64_t kTcFusedMinN = 256;
 
 struct TcFused {
-    float *wp_hi[2], *wp_lo[2], *lp_hi, *lp_lo, *xs_hi[2], *xs_lo[2], *d0_hi, *d0_lo, *d1_hi, *d1_lo;
+    float *wp_hi[2], *wp_lo[2], *lp_hi, *lp_lo, *xs_hi[3], *xs_lo[3], *d0_hi, *d0_lo, *d1_hi, *d1_lo;
     int64_t ra, rx;
 };
 
@@ -422,7 +426,7 @@ TcFused tc_fused_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
     }
     f.lp_hi = take(A);
     f.lp_lo = take(A);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
         f.xs_hi[i] = take(X);
         f.xs_lo[i] = take(X);
     }
@@ -451,7 +455,7 @@ int tc_w_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t n
     return tc_problem(q, f.d1_hi, f.d1_lo, nb, f.lp_hi, f.lp_lo, f.ra, nb, g);
 }
 
-// The apply of block b over its block row (R_b split in xs[b & 1]); the D_b^-1
+// The apply of block b over its block row (R_b split in xs[b % 3]); the D_b^-1
 // rows go to (dh, dl).
 int tc_x_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t n, int64_t nb, const float *W,
                  float *B, int64_t ldb, float gamma, float *dh, float *dl, cudaStream_t st) {
@@ -462,7 +466,7 @@ int tc_x_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t n
     g.beta_zero = 1;
     g.gamma = gamma;
     g.a_lower = 1;
-    return tc_problem(q, dh, dl, nb, f.xs_hi[b & 1], f.xs_lo[b & 1], f.rx, nb, g);
+    return tc_problem(q, dh, dl, nb, f.xs_hi[b % 3], f.xs_lo[b % 3], f.rx, nb, g);
 }
 
 }  // namespace
@@ -476,33 +480,38 @@ bool tc_fused_usable(int64_t m, int64_t n, int64_t nb) {
 
 size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb) {
     const int64_t ra = round_rows(m), rx = round_rows(n);
-    return (size_t)(6 * round256(ra * nb * 4) + 4 * round256(rx * nb * 4) + 4 * round256(nb * nb * 4));
+    return (size_t)(6 * round256(ra * nb * 4) + 6 * round256(rx * nb * 4) + 4 * round256(nb * nb * 4));
 }
 
-// W_0 = L_panel_0 D_0^-1, before step 0.
-int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, void *panels,
-                     cudaStream_t st) {
+// W_0 = L_panel_0 D_0^-1 and the split of R_0, before step 0.
+int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
+                     int64_t ldb, void *panels, cudaStream_t st) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
+    int rc = split_rows(B, ldb, n, nb, f.xs_hi[0], f.xs_lo[0], nb, st);  // columns of R_0
+    if (rc) return rc;
     TcLaunch P;
-    const int rc = tc_w_problem(P.p[0], f, 0, m, nb, L, lda, W, st);
+    rc = tc_w_problem(P.p[0], f, 0, m, nb, L, lda, W, st);
     return rc ? rc : tc_launch(P, 1, st);
 }
 
-// Step t: split R_t, then one launch of update t, W_{t+1} and apply t-1 (the
-// last step: apply t and apply t-1).  alpha enters through block 0.
+// Step t: one launch of update t (leaving R_{t+1} split), W_{t+1} and apply
+// t-1; the last step: apply t and apply t-1.  alpha enters through block 0.
 int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
                   float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
-    const int64_t tb = (m + nb - 1) / nb, r0 = t * nb, mb = (m - r0 < nb) ? m - r0 : nb;
-    int rc = split_rows(B + r0, ldb, n, mb, f.xs_hi[t & 1], f.xs_lo[t & 1], nb, st);  // columns of R_t
-    if (rc) return rc;
+    const int64_t tb = (m + nb - 1) / nb, r0 = t * nb;
+    int rc;
     TcLaunch P;
     int np = 0;
     if (t + 1 < tb) {
         TcArgs g = tc_args(m - r0 - nb, n, nb, B + r0 + nb, ldb);
         g.beta = t == 0 ? alpha : 1.f;
         g.gamma = t == 0 ? -alpha : -1.f;
-        if ((rc = tc_problem(P.p[np++], f.wp_hi[t & 1], f.wp_lo[t & 1], f.ra, f.xs_hi[t & 1], f.xs_lo[t & 1], f.rx,
+        g.xhi = f.xs_hi[(t + 1) % 3];
+        g.xlo = f.xs_lo[(t + 1) % 3];
+        g.ldxs = nb;
+        g.xrows = nb;
+        if ((rc = tc_problem(P.p[np++], f.wp_hi[t & 1], f.wp_lo[t & 1], f.ra, f.xs_hi[t % 3], f.xs_lo[t % 3], f.rx,
                              nb, g)))
             return rc;
         if (r0 + 2 * nb < m && (rc = tc_w_problem(P.p[np++], f, t + 1, m, nb, L, lda, W, st))) return rc;

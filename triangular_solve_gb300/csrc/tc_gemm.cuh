@@ -56,7 +56,8 @@ constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYT
 
 // out = beta*C + gamma*(A X) (beta_zero: out = gamma*(A X), C not read),
 // stored to C; with xhi set, out is also stored split (TF32 head/tail) and
-// K-major, xhi[col * ldxs + row], as the X operand of a later product.
+// K-major, xhi[col * ldxs + row], as the X operand of a later product, for
+// the rows below xrows.
 // a_lower: A is lower triangular, so a row tile stops its K loop at its last
 // row (a_lower = 2: K interleaves real and imaginary parts, two K per row).
 // cplx: the product is the real form of a complex one, output columns 2j
@@ -75,7 +76,7 @@ struct TcArgs {
     float beta, beta_im, gamma, gamma_im;
     int beta_zero, a_lower, a_upper, cplx;
     float *xhi, *xlo;
-    int64_t ldxs;
+    int64_t ldxs, xrows;
 };
 
 // One launch computes up to kTcMaxProblems independent products: their tiles
@@ -341,7 +342,10 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
             const int64_t ldc = g.ldc, N = g.N;
             const float beta = g.beta, gamma = g.gamma;
             const bool cplx = g.cplx != 0, load_c = !g.beta_zero && row_ok;
-            const bool plain_full = !cplx && g.xhi == nullptr && n0 + TC_BN <= N;
+            const bool real_full = !cplx && n0 + TC_BN <= N;  // a full column tile of a real product
+            float *const xhi = g.xhi, *const xlo = g.xlo;
+            const int64_t ldxs = g.ldxs;
+            const bool emit = xhi != nullptr && gr < g.xrows;  // this row also goes out split
             float cnext[32];
             // element (gr, gc) of C
             auto coff = [&](int64_t gc) -> int64_t {
@@ -352,7 +356,7 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
                 if (!load_c) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[j] = 0.f;
-                } else if (plain_full) {
+                } else if (real_full) {
                     const float *cp = C + gc0 * ldc + gr;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[j] = cp[j * ldc];
@@ -406,12 +410,12 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
                             const float orr = fmaf(beta, cr, fmaf(-beta_im, ci, ar));
                             const float oi = fmaf(beta, ci, fmaf(beta_im, cr, ai));
                             *reinterpret_cast<float2 *>(C + coff(gc)) = make_float2(orr, oi);
-                            if (g.xhi) {
-                                const int64_t re_row = gc * g.ldxs, im_row = re_row + g.ldxs, half = g.ldxs / 2;
+                            if (emit) {
+                                const int64_t re_row = gc * ldxs, im_row = re_row + ldxs, half = ldxs / 2;
                                 auto put = [&](int64_t o, float x) {
                                     const float h = to_tf32(x);
-                                    g.xhi[o] = h;
-                                    g.xlo[o] = to_tf32(x - h);
+                                    xhi[o] = h;
+                                    xlo[o] = to_tf32(x - h);
                                 };
                                 put(re_row + gr, orr);
                                 put(re_row + half + gr, -oi);
@@ -420,20 +424,29 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
                             }
                         }
                     }
-                } else if (row_ok && plain_full) {
+                } else if (row_ok && real_full && C && !emit) {
                     float *cp = C + (n0 + chunk * 32) * ldc + gr;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) cp[j * ldc] = fmaf(beta, ccur[j], gamma * __uint_as_float(v[j]));
+                } else if (row_ok && real_full && C) {
+                    const int64_t gc0 = n0 + chunk * 32;
+                    float *cp = C + gc0 * ldc + gr, *hp = xhi + gc0 * ldxs + gr, *lp = xlo + gc0 * ldxs + gr;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float o = fmaf(beta, ccur[j], gamma * __uint_as_float(v[j]));
+                        const float h = to_tf32(o);
+                        cp[j * ldc] = o;
+                        hp[j * ldxs] = h;
+                        lp[j * ldxs] = to_tf32(o - h);
+                    }
                 } else if (row_ok) {
-                    float *const xhi = g.xhi, *const xlo = g.xlo;
-                    const int64_t ldxs = g.ldxs;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int64_t gc = n0 + chunk * 32 + j;
                         if (gc < N) {
                             const float o = fmaf(beta, ccur[j], gamma * __uint_as_float(v[j]));
                             if (C) C[gc * ldc + gr] = o;
-                            if (xhi) {
+                            if (emit) {
                                 const float h = to_tf32(o);
                                 xhi[gc * ldxs + gr] = h;
                                 xlo[gc * ldxs + gr] = to_tf32(o - h);
