@@ -159,6 +159,11 @@ int split_rows(const float *src, int64_t ks, int64_t R, int64_t Kc, float *hi, f
     return launch_status();
 }
 
+// The products run on CTA pairs (tc_gemm_pair_kernel): 256-row output
+// tiles, each CTA loading 128 rows of A and of X.
+constexpr int kTcRowsPerTile = TC2_PAIR_M;
+constexpr int kTcXBox = TC_BN / 2;
+
 int sm_count() {
     static int sms = 0;
     if (sms == 0) {
@@ -179,10 +184,10 @@ int tc_problem(TcProblem &q, const float *a_hi, const float *a_lo, int64_t a_row
     int rc;
     if ((rc = make_map(&q.a_hi, a_hi, a_rows, g.K, ld, TC_BM))) return rc;
     if ((rc = make_map(&q.a_lo, a_lo, a_rows, g.K, ld, TC_BM))) return rc;
-    if ((rc = make_map(&q.x_hi, x_hi, x_rows, g.K, ld, TC_BN))) return rc;
-    if ((rc = make_map(&q.x_lo, x_lo, x_rows, g.K, ld, TC_BN))) return rc;
+    if ((rc = make_map(&q.x_hi, x_hi, x_rows, g.K, ld, kTcXBox))) return rc;
+    if ((rc = make_map(&q.x_lo, x_lo, x_rows, g.K, ld, kTcXBox))) return rc;
     q.g = g;
-    q.tiles_m = (int)((g.M + TC_BM - 1) / TC_BM);
+    q.tiles_m = (int)((g.M + kTcRowsPerTile - 1) / kTcRowsPerTile);
     q.tiles_n = (int)((g.N + TC_BN - 1) / TC_BN);
     q.nk = (int)((g.K + TC_BK - 1) / TC_BK);
     return TRSM_SUCCESS;
@@ -203,12 +208,24 @@ int tc_launch(TcLaunch &P, int np, cudaStream_t st) {
     if (tiles == 0) return TRSM_SUCCESS;
     if (tiles > INT32_MAX) return TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidValue;
     P.ntiles = (int)tiles;
-    const cudaError_t e =
-        cudaFuncSetAttribute(tc_update_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
-    if (e != cudaSuccess) return cuda_status(e);
-    const int sms = sm_count();
-    const unsigned ctas = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
-    tc_update_f32_kernel<<<ctas, 192, TC_SMEM, st>>>(P);
+    static int pairs = 0;  // CTA pairs resident at once (one CTA per SM)
+    if (pairs == 0) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC2_SMEM);
+        if (e != cudaSuccess) return cuda_status(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+        cfg.blockDim = dim3(192);
+        cfg.dynamicSmemBytes = TC2_SMEM;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = sm_count() / 2;
+        }
+        pairs = n;
+    }
+    const unsigned ctas = 2u * (unsigned)(tiles < pairs ? tiles : pairs);  // persistent
+    tc_gemm_pair_kernel<<<ctas, 192, TC2_SMEM, st>>>(P);
     return launch_status();
 }
 

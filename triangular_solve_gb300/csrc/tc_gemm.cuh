@@ -7,27 +7,31 @@
 //
 // f32 accuracy from TF32 tensor cores: each operand is split into a TF32
 // head and a TF32 tail (a = hi + lo, hi = tf32(a), lo = tf32(a - hi)) by a
-// preprocessing pass, and the product is accumulated in FP32 as
+// preprocessing pass (or by the epilogue that produced it), and the product
+// is accumulated in FP32 as
 //     A_hi X_hi + A_hi X_lo + A_lo X_hi
 // (the dropped A_lo X_lo term is ~2^-22 relative).
 //
-// Persistent kernel, one CTA per SM, each CTA taking 128 x 256 output tiles
-// in turn (of up to three independent products per launch), with six warps:
-//   warp 0  TMA producer: 2-D tensor loads of the four operand tiles of a
-//           16-deep K slab into a four-stage shared-memory ring (64-byte
-//           swizzle), completion counted on the stage's "full" mbarrier;
+// Persistent kernel on CTA pairs (clusters of two, tcgen05 cta_group::2):
+// each pair takes 256 x 256 output tiles in turn (of up to three independent
+// products per launch); each CTA of the pair holds 128 rows of A and 128
+// rows of X per K slab, and six warps:
+//   warp 0  TMA producer: 2-D tensor loads of its four operand halves of a
+//           16-deep K slab into a six-stage shared-memory ring (64-byte
+//           swizzle), completion counted on the even CTA's "full" mbarrier;
 //           the ring runs on from one tile to the next;
-//   warp 1  MMA issuer: one elected thread issues tcgen05.mma (kind::tf32,
-//           M = 128, N = 256, K = 8) into one of two FP32 accumulators in
-//           tensor memory (2 x 256 columns); tcgen05.commit frees each stage
-//           and signals "accumulator full";
+//   warp 1  (even CTA) MMA issuer: one elected thread issues the pair's
+//           tcgen05.mma (kind::tf32, M = 256, N = 256, K = 8) into one of two
+//           FP32 accumulators in tensor memory (2 x 256 columns in each CTA);
+//           tcgen05.commit frees each stage and signals "accumulator full" in
+//           both CTAs;
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, release of the
-//           accumulator, then the output straight to global memory
-//           (coalesced per column) while the MMAs of the next tile run.
+//           accumulator to the even CTA, then the output straight to global
+//           memory (coalesced per column) while the MMAs of the next tile run.
 // Every mbarrier wait is bounded: when a wait expires the kernel records
 // TRSM_ERR_DEVICE_TIMEOUT in a device status word and the CTA unwinds
-// (no hang): it waits (bounded) for its TMA loads and MMAs in flight, then
-// releases its tensor memory.
+// (no hang): it waits (bounded) for the loads and MMAs in flight, meets its
+// peer at the cluster barrier, then releases its tensor memory.
 #pragma once
 
 #include <cuda.h>
@@ -38,21 +42,14 @@
 
 namespace trsm {
 
-// K depth of a stage: 16 (64-byte rows, 64-byte swizzle, four stages) or 32
-// (128-byte rows and swizzle, two stages); the same 192 KB of ring either way,
-// but shallower stages let the producer run further ahead of the MMAs
-// (measured on GB300: 16 is 1.5-10% faster on the blocked solves).
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 16, TC_STAGES = TC_BK == 16 ? 4 : 2;
+// Tile shape: 128 rows of A and 256 columns per CTA accumulator, K slabs of
+// 16 (64-byte K-major rows, 64-byte swizzle; measured on GB300: 32-deep
+// slabs with the 128-byte swizzle were 1.5-10% slower).
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 16;
 static_assert(TC_BK == 16 || TC_BK == 32, "stage depth");
 constexpr int kTileGroup = 8;  // row tiles per group of the tile order
-constexpr uint32_t TC_ROW_BYTES = TC_BK * 4;                          // a K-major tile row: the swizzle span
-constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 4;                    // 8 / 16 KB
-constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 4;                    // 16 / 32 KB
-constexpr uint32_t TC_STAGE_BYTES = 2 * TC_A_BYTES + 2 * TC_B_BYTES;  // 48 / 96 KB
-constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column FP32 accumulators
-constexpr uint32_t kTmemSlotOffset = 8u * (2 * TC_STAGES + 5);  // after the 2*TC_STAGES + 5 barriers
-static_assert(kTmemSlotOffset + 4 <= 128, "barriers and TMEM slot fit the 128-byte region");
-constexpr size_t TC_SMEM = 1024 /* alignment slack */ + TC_STAGES * TC_STAGE_BYTES + 128 /* barriers */;
+constexpr uint32_t TC_ROW_BYTES = TC_BK * 4;  // a K-major tile row: the swizzle span
+constexpr uint32_t TC_TMEM_COLS = 512;        // two 256-column FP32 accumulators
 
 // out = beta*C + gamma*(A X) (beta_zero: out = gamma*(A X), C not read),
 // stored to C; with xhi set, out is also stored split (TF32 head/tail) and
@@ -96,14 +93,6 @@ struct TcLaunch {
     int *status;  // device status word (0 = ok)
 };
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major tile with TC_ROW_BYTES-byte
 // rows and the matching swizzle (128 B: mode 2, 64 B: mode 4); 8-row groups
 // 8 * TC_ROW_BYTES apart.
@@ -126,23 +115,6 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int m, int n) {
            | ((uint32_t)(m >> 4) << 24); // M / 16
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-
-
-
 // Round to TF32, nearest (ties away from zero).
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t r;
@@ -150,44 +122,103 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(r);
 }
 
-// Persistent: one CTA per SM walks the output tiles t = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  (consecutive CTAs take consecutive row tiles of
-// one column tile, so they share the X_t tile in L2).  The operand ring runs
-// on across tile boundaries, and the accumulator alternates between two
-// 256-column halves of tensor memory: the MMA warp fills one while the
-// epilogue warps drain the other (acc_full / acc_empty barriers).
-__global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_constant__ TcLaunch P) {
+// ---------------------------------------------------------------------------
+// The CTA pair (tcgen05 cta_group::2): the two CTAs of a cluster compute one
+// 256 x 256 output tile.  Each holds 128 rows of A and 128 rows of X per
+// K slab (32 KB a stage instead of 48: six stages in the same 192 KB), the
+// pair's MMA (M = 256, N = 256, K = 8), issued by the even CTA, reads both
+// CTAs' shared memory and leaves each CTA its 128 rows x 256 columns of the
+// accumulator in its own tensor memory.
+//   producer (both CTAs)  loads its halves; the loads complete on the even
+//                         CTA's "full" barrier, which expects the pair's bytes;
+//   MMA (even CTA)        commits "empty" and "accumulator full" to both CTAs;
+//   epilogue (both CTAs)  drains its accumulator rows and arrives on the even
+//                         CTA's "accumulator empty" (eight warps).
+// Against one CTA per 128 x 256 tile, the operand feed per SM drops by a
+// third and the tensor core's shared-memory reads per MMA from 12 KB to 8 KB
+// (measured on GB300: f32 m = 16384 17.6 -> 16.0 ms, c64 60.3 -> 53.2 ms).
+// ---------------------------------------------------------------------------
+constexpr int TC2_STAGES = 6;
+constexpr uint32_t TC2_A_BYTES = TC_BM * TC_BK * 4;        // 128 rows of A per CTA
+constexpr uint32_t TC2_B_BYTES = (TC_BN / 2) * TC_BK * 4;  // 128 rows of X per CTA
+constexpr uint32_t TC2_STAGE_BYTES = 2 * TC2_A_BYTES + 2 * TC2_B_BYTES;
+constexpr uint32_t kTc2BarBytes = 256;
+constexpr uint32_t kTc2TmemSlot = 8u * (2 * TC2_STAGES + 5);
+static_assert(kTc2TmemSlot + 4 <= kTc2BarBytes, "barriers and TMEM slot fit their region");
+constexpr size_t TC2_SMEM = 1024 + TC2_STAGES * TC2_STAGE_BYTES + kTc2BarBytes;
+constexpr int TC2_PAIR_M = 2 * TC_BM;  // output rows of a pair tile
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
+}
+// 2-D tile load into this CTA's shared memory, completing on a barrier of
+// either CTA of the pair (cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on the barrier at this offset in both CTAs of the pair once the
+// pair's MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+            bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcLaunch P) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte alignment for the swizzled tiles
     unsigned char *sbase = smem_raw + (base - raw);
-    const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;
-    // barrier region: full[TC_STAGES], empty[TC_STAGES], acc_full[2], acc_empty[2], drain, then the TMEM slot
+    const uint32_t bars = base + TC2_STAGES * TC2_STAGE_BYTES;
     auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 8u * (TC_STAGES + s); };
-    auto acc_full = [&](int a) { return bars + 8u * (2 * TC_STAGES + a); };
-    auto acc_empty = [&](int a) { return bars + 8u * (2 * TC_STAGES + 2 + a); };
-    const uint32_t drain = bars + 8u * (2 * TC_STAGES + 4);  // last commit of the MMA thread
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC_STAGES * TC_STAGE_BYTES + kTmemSlotOffset);
+    auto empty = [&](int s) { return bars + 8u * (TC2_STAGES + s); };
+    auto acc_full = [&](int a) { return bars + 8u * (2 * TC2_STAGES + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (2 * TC2_STAGES + 2 + a); };
+    const uint32_t drain = bars + 8u * (2 * TC2_STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TC2_STAGES * TC2_STAGE_BYTES + kTc2TmemSlot);
     __shared__ int abort_flag;
-    // the problems' arguments and tile counts, staged once: the tile loops
-    // index them by problem, and a dynamically indexed kernel parameter is a
-    // generic load on every use
     __shared__ TcArgs s_args[kTcMaxProblems];
-    __shared__ int4 s_tiles[kTcMaxProblems];  // tile_begin, tiles_m, tiles_n, nk
+    __shared__ int4 s_tiles[kTcMaxProblems];  // tile_begin, tiles_m (pair rows), tiles_n, nk
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = (int)blockIdx.x >> 1, npairs = (int)gridDim.x >> 1;
     const int ntiles = P.ntiles, np = P.np;
-    // Tile t -> (problem, row tile, column tile).  Within a problem the order
-    // is grouped: kTileGroup row tiles walk all column tiles together, so a
-    // wave of CTAs shares a few A tiles and a few X tiles in L2 instead of
-    // streaming the whole A panel once per column tile (the operand panels of
-    // large solves exceed L2).
-    // Triangular A alone in a launch (the block apply): the row tiles' K
-    // extents grow with the row, and with one group of row tiles a CTA would
-    // meet the same row tile in every round; reversing the row order on odd
-    // rounds pairs heavy with light tiles.  Only when each round holds whole
-    // column groups (then the mapping stays one-to-one).
     auto tile_of = [&](int t, int &pq, int &tm, int &tn) {
         pq = 0;
         while (pq + 1 < np && t >= s_tiles[pq + 1].x) ++pq;
@@ -198,15 +229,11 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
         const int gsize = min(kTileGroup, q.y - grp * kTileGroup);
         tm = grp * kTileGroup + rem % gsize;
         tn = rem / gsize;
-        const bool flip = np == 1 && s_args[0].a_lower && q.y <= kTileGroup && (int)gridDim.x % q.y == 0;
-        if (flip && ((t / (int)gridDim.x) & 1)) tm = q.y - 1 - tm;
     };
-    // K slabs [kb0, kb1) of row tile m0 of problem pq: a triangular A has
-    // zeros past (lower) or before (upper) the tile's rows
     auto k_range = [&](int pq, int m0, int &kb0, int &kb1) {
         const int nk = s_tiles[pq].w, lower = s_args[pq].a_lower;
         kb0 = s_args[pq].a_upper ? m0 / TC_BK : 0;
-        kb1 = lower ? min(nk, lower * (m0 + TC_BM) / TC_BK) : nk;
+        kb1 = lower ? min(nk, lower * (m0 + TC2_PAIR_M) / TC_BK) : nk;
     };
 
     if (threadIdx.x < np) {
@@ -216,25 +243,26 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
     }
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int s = 0; s < TC_STAGES; ++s) {
+        for (int s = 0; s < TC2_STAGES; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(acc_full(a), 1);
-            mbar_init(acc_empty(a), 4);  // one arrival per epilogue warp
+            mbar_init(acc_empty(a), 8);  // four epilogue warps in each CTA
         }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
                      "r"(TC_TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
     __syncthreads();
+    cluster_sync();  // the peer's barriers exist before anything signals them
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     const uint32_t tmem = *tmem_slot;
     auto aborted = [&]() { return *(volatile int *)&abort_flag != 0; };
@@ -246,39 +274,40 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
     if (warp == 0) {
         if (lane == 0) {
             int it = 0;
-            for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x) {
+            for (int t = pair; t < ntiles && !aborted(); t += npairs) {
                 int pq, tm, tn;
                 tile_of(t, pq, tm, tn);
                 const TcProblem &q = P.p[pq];
-                const int m0 = tm * TC_BM, n0 = tn * TC_BN;
+                const int m0 = tm * TC2_PAIR_M, n0 = tn * TC_BN;
+                const int ya = m0 + TC_BM * (int)rank, yx = n0 + (TC_BN / 2) * (int)rank;
                 int kb0, kb1;
                 k_range(pq, m0, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = it % TC_STAGES;
-                    if (it >= TC_STAGES && !mbar_wait(empty(s), ((it / TC_STAGES) - 1) & 1)) {
+                    const int s = it % TC2_STAGES;
+                    if (it >= TC2_STAGES && !mbar_wait(empty(s), ((it / TC2_STAGES) - 1) & 1)) {
                         fail();
                         break;
                     }
-                    const uint32_t st = base + s * TC_STAGE_BYTES;
-                    mbar_expect_tx(full(s), TC_STAGE_BYTES);
+                    if (leader) mbar_expect_tx(full(s), 2 * TC2_STAGE_BYTES);
+                    const uint32_t st = base + s * TC2_STAGE_BYTES, fb = map_to_rank(full(s), 0);
                     const int kx = kb * TC_BK;
-                    tma_load_2d(st, &q.a_hi, kx, m0, full(s));
-                    tma_load_2d(st + TC_A_BYTES, &q.a_lo, kx, m0, full(s));
-                    tma_load_2d(st + 2 * TC_A_BYTES, &q.x_hi, kx, n0, full(s));
-                    tma_load_2d(st + 2 * TC_A_BYTES + TC_B_BYTES, &q.x_lo, kx, n0, full(s));
+                    tma_load_2d_pair(st, &q.a_hi, kx, ya, fb);
+                    tma_load_2d_pair(st + TC2_A_BYTES, &q.a_lo, kx, ya, fb);
+                    tma_load_2d_pair(st + 2 * TC2_A_BYTES, &q.x_hi, kx, yx, fb);
+                    tma_load_2d_pair(st + 2 * TC2_A_BYTES + TC2_B_BYTES, &q.x_lo, kx, yx, fb);
                 }
             }
-            if (aborted()) {
-                // loads nobody consumed must land before the CTA's shared memory goes away
-                for (int j = (it > TC_STAGES ? it - TC_STAGES : 0); j < it; ++j)
-                    if (!mbar_wait(full(j % TC_STAGES), (j / TC_STAGES) & 1)) record_timeout(P.status);
+            if (aborted() && leader) {
+                // the pair's loads counted on these barriers land before shared memory goes away
+                for (int j = (it > TC2_STAGES ? it - TC2_STAGES : 0); j < it; ++j)
+                    if (!mbar_wait(full(j % TC2_STAGES), (j / TC2_STAGES) & 1)) record_timeout(P.status);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = tf32_idesc(TC_BM, TC_BN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = tf32_idesc(TC2_PAIR_M, TC_BN);
             int it = 0, i = 0;
-            for (int t = blockIdx.x; t < ntiles && !aborted(); t += gridDim.x, ++i) {
+            for (int t = pair; t < ntiles && !aborted(); t += npairs, ++i) {
                 const int a = i & 1;
                 if (i >= 2 && !mbar_wait(acc_empty(a), ((i >> 1) - 1) & 1)) {
                     fail();
@@ -289,50 +318,46 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
                 int pq, tm, tn;
                 tile_of(t, pq, tm, tn);
                 int kb0, kb1;
-                k_range(pq, tm * TC_BM, kb0, kb1);
+                k_range(pq, tm * TC2_PAIR_M, kb0, kb1);
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = it % TC_STAGES;
-                    if (!mbar_wait(full(s), (it / TC_STAGES) & 1)) {
+                    const int s = it % TC2_STAGES;
+                    if (!mbar_wait(full(s), (it / TC2_STAGES) & 1)) {
                         fail();
                         ok = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-                    const uint32_t st = base + s * TC_STAGE_BYTES;
+                    const uint32_t st = base + s * TC2_STAGE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < TC_BK / 8; ++kk) {
                         const uint64_t a_hi = tile_desc(st + kk * 32);
-                        const uint64_t a_lo = tile_desc(st + TC_A_BYTES + kk * 32);
-                        const uint64_t x_hi = tile_desc(st + 2 * TC_A_BYTES + kk * 32);
-                        const uint64_t x_lo = tile_desc(st + 2 * TC_A_BYTES + TC_B_BYTES + kk * 32);
-                        mma_tf32(d, a_hi, x_hi, idesc, kb != kb0 || kk != 0);
-                        mma_tf32(d, a_hi, x_lo, idesc, 1);
-                        mma_tf32(d, a_lo, x_hi, idesc, 1);
+                        const uint64_t a_lo = tile_desc(st + TC2_A_BYTES + kk * 32);
+                        const uint64_t x_hi = tile_desc(st + 2 * TC2_A_BYTES + kk * 32);
+                        const uint64_t x_lo = tile_desc(st + 2 * TC2_A_BYTES + TC2_B_BYTES + kk * 32);
+                        mma_tf32_pair(d, a_hi, x_hi, idesc, kb != kb0 || kk != 0);
+                        mma_tf32_pair(d, a_hi, x_lo, idesc, 1);
+                        mma_tf32_pair(d, a_lo, x_hi, idesc, 1);
                     }
-                    mma_commit(empty(s));  // the stage is free once these MMAs have read it
+                    mma_commit_pair_both(empty(s));  // both CTAs' stage s is free once these MMAs have read it
                 }
-                mma_commit(acc_full(a));  // accumulator a complete (or abandoned)
+                mma_commit_pair_both(acc_full(a));  // accumulator a complete (or abandoned) in both CTAs
                 if (!ok) break;
             }
-            // every MMA issued here has finished before tensor memory is released
-            mma_commit(drain);
+            mma_commit_pair_local(drain);
             if (!mbar_wait(drain, 0)) record_timeout(P.status);
         }
     } else {
-        // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31.  A thread owns
-        // one row of a tile; C is read a 32-column chunk at a time into
-        // registers (32 loads in flight), the next chunk's loads are issued
-        // before the current chunk is written, and a tile's first chunk is
-        // fetched while its accumulator is still being computed.
+        // epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31 of this CTA's
+        // 128 accumulator rows
         const int quarter = warp & 3;
         int i = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        for (int t = pair; t < ntiles; t += npairs, ++i) {
             const int a = i & 1;
             int pq, tm, tn;
             tile_of(t, pq, tm, tn);
             const TcArgs &g = s_args[pq];
-            const int m0 = tm * TC_BM, n0 = tn * TC_BN;
+            const int m0 = tm * TC2_PAIR_M + TC_BM * (int)rank, n0 = tn * TC_BN;
             const int64_t gr = m0 + 32 * quarter + lane;
             const bool row_ok = gr < g.M;
             // loop invariants of the tile, hoisted: the column loops below
@@ -395,7 +420,7 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
                     // every TMEM read of accumulator a is done: hand it back
                     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty(a));
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(acc_empty(a), 0));
                 }
                 if (row_ok && cplx) {
                     const float beta_im = g.beta_im, gamma_im = g.gamma_im;
@@ -459,9 +484,10 @@ __global__ void __launch_bounds__(192, 1) tc_update_f32_kernel(const __grid_cons
     }
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
     __syncthreads();
+    cluster_sync();  // the pair's MMAs and loads are done with both CTAs' memory
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TC_TMEM_COLS)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
     }
 }
