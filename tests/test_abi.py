@@ -72,6 +72,13 @@ def test_workspace_bytes_lookahead_form(lib):
     per_block = 2 * r(m * nb * 4) + 4 * r(n * nb * 4)
     fused = 6 * r(1024 * nb * 4) + 6 * r(1024 * nb * 4) + 4 * r(nb * nb * 4)
     assert tg.trsm_llnn_workspace_bytes("f32", m, n, nb) == base + max(per_block, fused)
+    # c64 in real form: W' (m rows) twice, the L panel's X' (2m rows) once,
+    # R_t's X' (2n rows) three times, four NB x 2NB blocks; 2 NB floats a row
+    base64 = r(4 * nb * nb * 8) + 2 * r(nb * 780 * 8)
+    per_block64 = 2 * r(m * 2 * nb * 4) + 4 * r(2 * n * 2 * nb * 4)
+    fused64 = 4 * r(1024 * 2 * nb * 4) + 2 * r(2048 * 2 * nb * 4) + 6 * r(2048 * 2 * nb * 4) + \
+        4 * r(nb * 2 * nb * 4)
+    assert tg.trsm_llnn_workspace_bytes("c64", m, n, nb) == base64 + max(per_block64, fused64)
     # an 8-row last block keeps the per-block flow
     assert tg.trsm_llnn_workspace_bytes("f32", 520, 300, 256) == \
         r(3 * nb * nb * 4) + 2 * r(nb * 300 * 4) + 2 * r(520 * nb * 4) + 4 * r(300 * nb * 4)

@@ -159,14 +159,17 @@ def test_tensor_core_products_ragged(env, dtype, nb, m, n):
     (1280, 600, 128, 3),   # ten blocks, ragged column tiles
     (3000, 512, 512, 0),   # 440-row last block
 ])
-def test_lookahead_flow_edges(env, m, n, nb, ld_pad):
-    """f32 look-ahead form (update t, the scaled panel L_panel D^-1 of block
-    t+1 and the apply of block t-1 in one launch): block counts, last-block
-    sizes, column raggedness and leading dimensions at its edges."""
-    L, B = ti.generate("f32", m, n, 1, kind="ddm", seed=m + n + nb)
-    xg, xr = _ex_solve(env, "f32", L, B, -0.75, nb, lda=m + ld_pad, ldb=m + ld_pad)
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
+def test_lookahead_flow_edges(env, dtype, m, n, nb, ld_pad):
+    """Look-ahead form (update t, the scaled panel L_panel D^-1 of block t+1
+    and the apply of block t-1 in one launch; c64 in real form with
+    interleaved K): block counts, last-block sizes, column raggedness and
+    leading dimensions at its edges, complex alpha."""
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + n + nb)
+    alpha = (-0.75 + 0.5j) if ti.IS_COMPLEX[dtype] else -0.75
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, nb, lda=m + ld_pad, ldb=m + ld_pad)
     assert env["tg"].trsm_device_status() == 0
-    assert_parity("f32", xg, xr, f"look-ahead m={m} n={n} nb={nb}")
+    assert_parity(dtype, xg, xr, f"look-ahead {dtype} m={m} n={n} nb={nb}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "c64"])

@@ -240,6 +240,22 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
             return TRSM_SUCCESS;
         }
     }
+    if constexpr (std::is_same<T, float2>::value) {
+        if (tc_panels && tc_fused_usable_c64(m, n, nb)) {
+            // the look-ahead form in real form (tc_gemm.cu), phases as for f32
+            timer.begin();
+            rc = tc_fused_prepare_c64(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st);
+            for (int64_t t = 0; !rc && t + 1 < tb; ++t)
+                rc = tc_fused_step_c64(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            if (rc || (rc = timer.end(2))) return rc;
+            timer.begin();
+            rc = tc_fused_step_c64(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            if (rc || (rc = timer.end(1))) return rc;
+            if (a.ms)
+                for (int q = 0; q < 3; ++q) a.ms[q] = timer.acc[q];
+            return TRSM_SUCCESS;
+        }
+    }
     for (int64_t t = 0; t < tb; ++t) {
         const int64_t r0 = t * nb;
         const int64_t mb = (m - r0 < nb) ? m - r0 : nb;

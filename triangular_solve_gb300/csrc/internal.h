@@ -72,7 +72,8 @@ inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 // tc_fused_bytes).
 // c64 adds the real-form operands of its tensor-core products
 // (tc_panel_bytes_c64: A' = m x 2nb, X' = 2n x 2nb and the split X_t' the
-// apply leaves for the update, two copies each).
+// apply leaves for the update, two copies each; or the look-ahead panels,
+// tc_fused_bytes_c64, when that form applies and needs more).
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb);
 size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb);
 inline size_t blocked_workspace_bytes(int dtype, int64_t m, int64_t n, int64_t nb) {
@@ -106,6 +107,13 @@ int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t l
                      int64_t ldb, void *panels, cudaStream_t st);
 int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
                   float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st);
+// The same for c64, in real form with interleaved K (tc_gemm.cu).
+bool tc_fused_usable_c64(int64_t m, int64_t n, int64_t nb);
+size_t tc_fused_bytes_c64(int64_t m, int64_t n, int64_t nb);
+int tc_fused_prepare_c64(int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
+                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st);
+int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
+                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st);
 // Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).
 int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
                    const uint32_t *box, bool swizzle128);

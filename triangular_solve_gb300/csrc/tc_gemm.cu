@@ -251,6 +251,7 @@ TcArgs tc_args(int64_t M, int64_t N, int64_t K, float *C, int64_t ldc) {
     g.a_lower = 0;
     g.a_upper = 0;
     g.cplx = 0;
+    g.xmode = 0;
     g.xhi = g.xlo = nullptr;
     g.ldxs = 0;
     g.xrows = M;
@@ -300,7 +301,9 @@ static TcPanelsC64 tc_layout_c64(void *panels, int64_t m, int64_t n, int64_t nb)
 }
 
 size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb) {
-    return (size_t)(2 * round256(m * 2 * nb * 4) + 4 * round256(2 * n * 2 * nb * 4));
+    const size_t per_block = (size_t)(2 * round256(m * 2 * nb * 4) + 4 * round256(2 * n * 2 * nb * 4));
+    const size_t fused = tc_fused_usable_c64(m, n, nb) ? tc_fused_bytes_c64(m, n, nb) : 0;
+    return per_block > fused ? per_block : fused;
 }
 
 // c64 trailing update C = beta*C - A X (A column-major lda, all complex) as
@@ -343,11 +346,11 @@ int tc_apply_c64(int64_t mb, int64_t N, const float2 *Wt, int64_t nb, float2 *Bt
                  int64_t Mmax, void *panels, bool emit_split, cudaStream_t st) {
     const TcPanelsC64 p = tc_layout_c64(panels, Mmax, N, nb);
     split_c64_ai_kernel<<<dim3((unsigned)((mb + 31) / 32), (unsigned)((mb + 31) / 32)), dim3(32, 8), 0, st>>>(
-        Wt, nb, mb, mb, p.a_hi, p.a_lo);
+        Wt, nb, mb, mb, p.a_hi, p.a_lo, 2 * mb);
     int rc = launch_status();
     if (rc) return rc;
     split_c64_xi_kernel<<<dim3((unsigned)((mb + 127) / 128), (unsigned)(N < 65535 ? N : 65535)), 128, 0, st>>>(
-        Bt, ldb, mb, N, p.x_hi, p.x_lo);
+        Bt, ldb, mb, N, p.x_hi, p.x_lo, 2 * mb);
     if ((rc = launch_status())) return rc;
     TcArgs g = tc_args(mb, 2 * N, 2 * mb, reinterpret_cast<float *>(Bt), 2 * ldb);
     g.beta_zero = 1;
@@ -538,6 +541,156 @@ int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, i
     }
     if (t >= 1 &&
         (rc = tc_x_problem(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : 1.f, f.d0_hi, f.d0_lo, st)))
+        return rc;
+    return tc_launch(P, np, st);
+}
+
+// ---------------------------------------------------------------------------
+// The look-ahead form for c64, in real form with interleaved K throughout
+// (k' = 2k real part, 2k + 1 imaginary part), so that the update and the
+// apply read the same split block row:
+//   A' of W_t      row i = [Re W(i,0), Im W(i,0), Re W(i,1), ...]   (ra x 2nb)
+//   X' of R_t      rows 2j, 2j+1 of column j, interleaved (xmode 1)  (2rx x 2nb)
+//   X' of L_panel^T rows 2i, 2i+1 of panel row i, interleaved        (2ra x 2nb)
+//   A' of D^-1 / D^-T rows, interleaved                              (nb x 2nb)
+// The W_{t+1}^T product leaves W_{t+1} transposed in A' layout (xmode 2);
+// update t leaves R_{t+1} in X' layout (xmode 1).
+// ---------------------------------------------------------------------------
+namespace {
+
+struct TcFusedC64 {
+    float *wp_hi[2], *wp_lo[2], *lp_hi, *lp_lo, *xs_hi[3], *xs_lo[3], *d0_hi, *d0_lo, *d1_hi, *d1_lo;
+    int64_t ra, rx;
+};
+
+TcFusedC64 tc_fused_layout_c64(void *panels, int64_t m, int64_t n, int64_t nb) {
+    TcFusedC64 f;
+    f.ra = round_rows(m);
+    f.rx = round_rows(n);
+    const size_t A = round256(f.ra * 2 * nb * 4), L = round256(2 * f.ra * 2 * nb * 4),
+                 X = round256(2 * f.rx * 2 * nb * 4), D = round256(nb * 2 * nb * 4);
+    char *c = static_cast<char *>(panels);
+    auto take = [&](size_t bytes) {
+        float *p = reinterpret_cast<float *>(c);
+        c += bytes;
+        return p;
+    };
+    for (int i = 0; i < 2; ++i) {
+        f.wp_hi[i] = take(A);
+        f.wp_lo[i] = take(A);
+    }
+    f.lp_hi = take(L);
+    f.lp_lo = take(L);
+    for (int i = 0; i < 3; ++i) {
+        f.xs_hi[i] = take(X);
+        f.xs_lo[i] = take(X);
+    }
+    f.d0_hi = take(D);
+    f.d0_lo = take(D);
+    f.d1_hi = take(D);
+    f.d1_lo = take(D);
+    return f;
+}
+
+int tc_w_problem_c64(TcProblem &q, const TcFusedC64 &f, int64_t b, int64_t m, int64_t nb, const float2 *L,
+                     int64_t lda, const float2 *W, cudaStream_t st) {
+    const int64_t r1 = b * nb, rows = m - r1 - nb;
+    split_c64_xt_kernel<<<dim3((unsigned)((rows + 31) / 32), (unsigned)((nb + 31) / 32)), dim3(32, 8), 0, st>>>(
+        L + r1 * lda + r1 + nb, lda, rows, nb, f.lp_hi, f.lp_lo, 2 * nb);
+    int rc = launch_status();
+    // rows of D_b^-T, interleaved: column r of the column-major D_b^-1 as float pairs
+    if (!rc) rc = split_rows(reinterpret_cast<const float *>(W + b * nb * nb), 2 * nb, nb, 2 * nb, f.d1_hi, f.d1_lo,
+                             2 * nb, st);
+    if (rc) return rc;
+    TcArgs g = tc_args(nb, 2 * rows, 2 * nb, nullptr, 0);
+    g.beta_zero = 1;
+    g.gamma = 1.f;
+    g.a_upper = 2;
+    g.cplx = 1;
+    g.xhi = f.wp_hi[b & 1];
+    g.xlo = f.wp_lo[b & 1];
+    g.ldxs = 2 * nb;
+    g.xmode = 2;
+    return tc_problem(q, f.d1_hi, f.d1_lo, nb, f.lp_hi, f.lp_lo, 2 * f.ra, 2 * nb, g);
+}
+
+int tc_x_problem_c64(TcProblem &q, const TcFusedC64 &f, int64_t b, int64_t m, int64_t n, int64_t nb,
+                     const float2 *W, float2 *B, int64_t ldb, float2 gamma, float *dh, float *dl, cudaStream_t st) {
+    const int64_t r0 = b * nb, mb = (m - r0 < nb) ? m - r0 : nb;
+    split_c64_ai_kernel<<<dim3((unsigned)((mb + 31) / 32), (unsigned)((mb + 31) / 32)), dim3(32, 8), 0, st>>>(
+        W + b * nb * nb, nb, mb, mb, dh, dl, 2 * nb);
+    const int rc = launch_status();
+    if (rc) return rc;
+    TcArgs g = tc_args(mb, 2 * n, 2 * mb, reinterpret_cast<float *>(B + r0), 2 * ldb);
+    g.beta_zero = 1;
+    g.gamma = gamma.x;
+    g.gamma_im = gamma.y;
+    g.a_lower = 2;
+    g.cplx = 1;
+    return tc_problem(q, dh, dl, nb, f.xs_hi[b % 3], f.xs_lo[b % 3], 2 * f.rx, 2 * nb, g);
+}
+
+}  // namespace
+
+bool tc_fused_usable_c64(int64_t m, int64_t n, int64_t nb) {
+    // The same shapes as f32, up to n = 8192.  Measured on GB300 (same box,
+    // NB 512): m = n = 8192 9.09 ms against 9.66 per block, m = n = 16384
+    // 65.1 against 63.9 -- once the split block row (2n x 2NB floats, head
+    // and tail: 268 MB at n = 16384) is twice the L2, the launch's extra
+    // panels of that size (R_{t+1} written, the L panel's X' read) cost what
+    // the folded apply saves.
+    return n <= 8192 && tc_fused_usable(m, n, nb);
+}
+
+size_t tc_fused_bytes_c64(int64_t m, int64_t n, int64_t nb) {
+    const int64_t ra = round_rows(m), rx = round_rows(n);
+    return (size_t)(4 * round256(ra * 2 * nb * 4) + 2 * round256(2 * ra * 2 * nb * 4) +
+                    6 * round256(2 * rx * 2 * nb * 4) + 4 * round256(nb * 2 * nb * 4));
+}
+
+int tc_fused_prepare_c64(int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
+                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st) {
+    const TcFusedC64 f = tc_fused_layout_c64(panels, m, n, nb);
+    split_c64_xi_kernel<<<dim3((unsigned)((nb + 127) / 128), (unsigned)(n < 65535 ? n : 65535)), 128, 0, st>>>(
+        B, ldb, nb, n, f.xs_hi[0], f.xs_lo[0], 2 * nb);  // R_0, interleaved X'
+    int rc = launch_status();
+    if (rc) return rc;
+    TcLaunch P;
+    rc = tc_w_problem_c64(P.p[0], f, 0, m, nb, L, lda, W, st);
+    return rc ? rc : tc_launch(P, 1, st);
+}
+
+int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
+                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st) {
+    const TcFusedC64 f = tc_fused_layout_c64(panels, m, n, nb);
+    const int64_t tb = (m + nb - 1) / nb, r0 = t * nb;
+    const float2 one = make_float2(1.f, 0.f);
+    int rc;
+    TcLaunch P;
+    int np = 0;
+    if (t + 1 < tb) {
+        TcArgs g = tc_args(m - r0 - nb, 2 * n, 2 * nb, reinterpret_cast<float *>(B + r0 + nb), 2 * ldb);
+        const float2 beta = t == 0 ? alpha : one;
+        g.beta = beta.x;
+        g.beta_im = beta.y;
+        g.gamma = -beta.x;
+        g.gamma_im = -beta.y;
+        g.cplx = 1;
+        g.xhi = f.xs_hi[(t + 1) % 3];
+        g.xlo = f.xs_lo[(t + 1) % 3];
+        g.ldxs = 2 * nb;
+        g.xrows = nb;
+        g.xmode = 1;
+        if ((rc = tc_problem(P.p[np++], f.wp_hi[t & 1], f.wp_lo[t & 1], f.ra, f.xs_hi[t % 3], f.xs_lo[t % 3],
+                             2 * f.rx, 2 * nb, g)))
+            return rc;
+        if (r0 + 2 * nb < m && (rc = tc_w_problem_c64(P.p[np++], f, t + 1, m, nb, L, lda, W, st))) return rc;
+    } else if ((rc = tc_x_problem_c64(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : one, f.d1_hi,
+                                      f.d1_lo, st))) {
+        return rc;
+    }
+    if (t >= 1 && (rc = tc_x_problem_c64(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : one, f.d0_hi,
+                                         f.d0_lo, st)))
         return rc;
     return tc_launch(P, np, st);
 }

@@ -64,14 +64,18 @@ constexpr uint32_t TC_TMEM_COLS = 512;        // two 256-column FP32 accumulator
 // split copy is the X' operand of tc_update_c64: row 2j = [Re | -Im],
 // row 2j+1 = [Im | Re], halves ldxs/2 apart.
 // a_upper: A is upper triangular, a row tile starts its K loop at its first
-// row.  C == nullptr (with beta_zero and xhi set): only the split copy is
-// stored.
+// row (a_upper = 2: interleaved K).  C == nullptr (with beta_zero and xhi
+// set): only the split copy is stored.  xmode picks the layout of a complex
+// split copy: 0 the X' rows above with [Re | Im] halves; 1 the same rows with
+// interleaved K (row 2j = [Re x_0, -Im x_0, Re x_1, ...], row 2j+1 =
+// [Im x_0, Re x_0, ...]); 2 the output transposed as the A' operand of a
+// later product, interleaved: xhi[j * ldxs + 2 * row + {0, 1}] = {Re, Im}.
 struct TcArgs {
     int64_t M, N, K;
     float *C;
     int64_t ldc;
     float beta, beta_im, gamma, gamma_im;
-    int beta_zero, a_lower, a_upper, cplx;
+    int beta_zero, a_lower, a_upper, cplx, xmode;
     float *xhi, *xlo;
     int64_t ldxs, xrows;
 };
@@ -232,7 +236,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     };
     auto k_range = [&](int pq, int m0, int &kb0, int &kb1) {
         const int nk = s_tiles[pq].w, lower = s_args[pq].a_lower;
-        kb0 = s_args[pq].a_upper ? m0 / TC_BK : 0;
+        kb0 = s_args[pq].a_upper * m0 / TC_BK;
         kb1 = lower ? min(nk, lower * (m0 + TC2_PAIR_M) / TC_BK) : nk;
     };
 
@@ -371,6 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             float *const xhi = g.xhi, *const xlo = g.xlo;
             const int64_t ldxs = g.ldxs;
             const bool emit = xhi != nullptr && gr < g.xrows;  // this row also goes out split
+            const int xmode = g.xmode;
             float cnext[32];
             // element (gr, gc) of C
             auto coff = [&](int64_t gc) -> int64_t {
@@ -434,18 +439,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                             const float ai = fmaf(gamma, pi, gamma_im * pr);
                             const float orr = fmaf(beta, cr, fmaf(-beta_im, ci, ar));
                             const float oi = fmaf(beta, ci, fmaf(beta_im, cr, ai));
-                            *reinterpret_cast<float2 *>(C + coff(gc)) = make_float2(orr, oi);
+                            if (C) *reinterpret_cast<float2 *>(C + coff(gc)) = make_float2(orr, oi);
                             if (emit) {
-                                const int64_t re_row = gc * ldxs, im_row = re_row + ldxs, half = ldxs / 2;
-                                auto put = [&](int64_t o, float x) {
-                                    const float h = to_tf32(x);
-                                    xhi[o] = h;
-                                    xlo[o] = to_tf32(x - h);
+                                auto put2 = [&](int64_t o, float x, float y) {  // a pair, 8-byte aligned
+                                    const float hx = to_tf32(x), hy = to_tf32(y);
+                                    *reinterpret_cast<float2 *>(xhi + o) = make_float2(hx, hy);
+                                    *reinterpret_cast<float2 *>(xlo + o) = make_float2(to_tf32(x - hx), to_tf32(y - hy));
                                 };
-                                put(re_row + gr, orr);
-                                put(re_row + half + gr, -oi);
-                                put(im_row + gr, oi);
-                                put(im_row + half + gr, orr);
+                                if (xmode == 2) {
+                                    put2((gc >> 1) * ldxs + 2 * gr, orr, oi);
+                                } else if (xmode == 1) {
+                                    const int64_t re_row = gc * ldxs, im_row = re_row + ldxs;
+                                    put2(re_row + 2 * gr, orr, -oi);
+                                    put2(im_row + 2 * gr, oi, orr);
+                                } else {
+                                    const int64_t re_row = gc * ldxs, im_row = re_row + ldxs, half = ldxs / 2;
+                                    auto put = [&](int64_t o, float x) {
+                                        const float h = to_tf32(x);
+                                        xhi[o] = h;
+                                        xlo[o] = to_tf32(x - h);
+                                    };
+                                    put(re_row + gr, orr);
+                                    put(re_row + half + gr, -oi);
+                                    put(im_row + gr, oi);
+                                    put(im_row + half + gr, orr);
+                                }
                             }
                         }
                     }
@@ -610,7 +628,7 @@ __global__ void split_c64_x_kernel(const float2 *__restrict__ src, int64_t ks, i
 //   X' row 2j = [Re X(0,j), -Im X(0,j), ...], row 2j+1 = [Im X(0,j), Re X(0,j), ...]
 //                                                      (X column-major, ks)
 __global__ void split_c64_ai_kernel(const float2 *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
-                                    float *__restrict__ hi, float *__restrict__ lo) {
+                                    float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
     __shared__ float2 tile[32][33];
     const int64_t r0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
     for (int q = threadIdx.y; q < 32; q += blockDim.y) {
@@ -623,7 +641,7 @@ __global__ void split_c64_ai_kernel(const float2 *__restrict__ src, int64_t ks, 
         if (r < R && k < Kc) {
             const float2 a = tile[threadIdx.x][q];
             const float hr = to_tf32(a.x), hi_ = to_tf32(a.y);
-            const int64_t o = r * 2 * Kc + 2 * k;
+            const int64_t o = r * ldd + 2 * k;
             *reinterpret_cast<float2 *>(hi + o) = make_float2(hr, hi_);
             *reinterpret_cast<float2 *>(lo + o) = make_float2(to_tf32(a.x - hr), to_tf32(a.y - hi_));
         }
@@ -631,18 +649,47 @@ __global__ void split_c64_ai_kernel(const float2 *__restrict__ src, int64_t ks, 
 }
 
 __global__ void split_c64_xi_kernel(const float2 *__restrict__ src, int64_t ks, int64_t Kc, int64_t N,
-                                    float *__restrict__ hi, float *__restrict__ lo) {
+                                    float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= Kc) return;
     for (int64_t j = blockIdx.y; j < N; j += gridDim.y) {
         const float2 x = src[j * ks + k];
         const float hr = to_tf32(x.x), hm = to_tf32(x.y);
         const float lr = to_tf32(x.x - hr), lm = to_tf32(x.y - hm);
-        const int64_t re = 2 * j * 2 * Kc + 2 * k, im = re + 2 * Kc;
+        const int64_t re = 2 * j * ldd + 2 * k, im = re + ldd;
         *reinterpret_cast<float2 *>(hi + re) = make_float2(hr, -hm);
         *reinterpret_cast<float2 *>(lo + re) = make_float2(lr, -lm);
         *reinterpret_cast<float2 *>(hi + im) = make_float2(hm, hr);
         *reinterpret_cast<float2 *>(lo + im) = make_float2(lm, lr);
+    }
+}
+
+// X' rows with interleaved K of the transpose of a column-major panel:
+// X(k, i) = src[i + k * ks] (i < R, k < Kc), so row 2i of the output is
+// [Re src(i, 0), -Im src(i, 0), Re src(i, 1), ...] and row 2i + 1 is
+// [Im src(i, 0), Re src(i, 0), ...] (row stride ldd floats).  32 x 32 tiles
+// through shared memory (src is read along i, the output written along k).
+__global__ void split_c64_xt_kernel(const float2 *__restrict__ src, int64_t ks, int64_t R, int64_t Kc,
+                                    float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    __shared__ float2 tile[32][33];
+    const int64_t i0 = (int64_t)blockIdx.x * 32, k0 = (int64_t)blockIdx.y * 32;
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t i = i0 + threadIdx.x, k = k0 + q;
+        tile[q][threadIdx.x] = (i < R && k < Kc) ? src[i + k * ks] : make_float2(0.f, 0.f);
+    }
+    __syncthreads();
+    for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+        const int64_t i = i0 + q, k = k0 + threadIdx.x;
+        if (i < R && k < Kc) {
+            const float2 x = tile[threadIdx.x][q];
+            const float hr = to_tf32(x.x), hm = to_tf32(x.y);
+            const float lr = to_tf32(x.x - hr), lm = to_tf32(x.y - hm);
+            const int64_t re = 2 * i * ldd + 2 * k, im = re + ldd;
+            *reinterpret_cast<float2 *>(hi + re) = make_float2(hr, -hm);
+            *reinterpret_cast<float2 *>(lo + re) = make_float2(lr, -lm);
+            *reinterpret_cast<float2 *>(hi + im) = make_float2(hm, hr);
+            *reinterpret_cast<float2 *>(lo + im) = make_float2(lm, lr);
+        }
     }
 }
 
