@@ -425,6 +425,42 @@ def run_large(torch, tg, dev, stream, peaks, reps=2):
     return res
 
 
+def trtri_bench(args):
+    """One JSON line per (type, m): the triangular inverse L^-1 through
+    trsm_trtri_lower (set to I, then the L X = I solve), CUDA events on the
+    launching stream, inputs resident; GFLOPS credit TRTRI's m^3/3 real flops
+    (x4 complex) and, beside it, the m^3 of the solve it runs."""
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    for d in args.sweep_dtypes.split(","):
+        for mm in [int(x) for x in args.sweep_ms.split(",")]:
+            L, _ = ti.generate(d, mm, 1, 1, kind="ddm")
+            a = torch.from_numpy(ti.to_storage(L, "col")).to(dev)
+            del L
+            x = torch.empty_like(a)
+            tg.trsm_trtri_lower(d, mm, a, mm, x, mm, stream)  # warm-up (and workspace pool)
+            times = []
+            for _ in range(max(args.sweep_reps, 1)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                tg.trsm_trtri_lower(d, mm, a, mm, x, mm, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.mean(times)
+            cplx = 4 if d in ("c64", "c128") else 1
+            print(json.dumps({"op": "trtri", "dtype": d, "m": mm, "ms": round(ms, 3),
+                              "gflops_trtri": round(cplx * mm ** 3 / 3 / (ms * 1e-3) / 1e9, 1),
+                              "gflops_solve": round(cplx * mm ** 3 / (ms * 1e-3) / 1e9, 1)}), flush=True)
+            del a, x
+            torch.cuda.empty_cache()
+
+
 def pipe_peaks():
     """TFLOP/s of dependent-free FMA loops on every SM: FP32 FMA, paired FP32
     FMA, FP64 FMA and the FP64 warp MMA (m8n8k4), three measurements each."""
@@ -601,6 +637,8 @@ def main():
     ap.add_argument("--dtypes", default="f32,f64,c64,c128",
                     help="subset of the step's types (profiling a single kernel)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--trtri", action="store_true",
+                    help="time the exported triangular inverse (trsm_trtri_lower) at --sweep-ms per --sweep-dtypes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -614,6 +652,9 @@ def main():
         return
     if args.pipe_peaks:
         pipe_peaks()
+        return
+    if args.trtri:
+        trtri_bench(args)
         return
     run_gb300(args, ws, rank, local)
 

@@ -170,6 +170,23 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
                       void *workspace, size_t ws_bytes, void *stream, float *ms);
 
 /*
+ * Triangular inverse (TRTRI, lower, non-unit):  Ainv = L^{-1}, the inverse
+ * of the lower triangle of A (m x m, lda >= max(1,m); the strictly upper part
+ * of A is never read), into Ainv (m x m, column-major, ldinv >= max(1,m)),
+ * whose strictly upper part is set to zero.  Computed as the solve
+ * L Ainv = I on `stream` (Ainv is set to the identity, then solved in place
+ * by the path trsm_llnn takes, with the same workspace allocation), so it
+ * costs the m^3 flops of that solve rather than TRTRI's m^3/3; the
+ * diagonal-block inverses of "Hierarchical Shared Memory-Aware Optimization
+ * for TRSM on GPU Platforms" are its first phase.  Ainv must not overlap A.
+ * A zero on the diagonal gives IEEE infinities / NaN, no status.
+ *
+ * Arguments: 1 dtype, 2 m, 3 A, 4 lda, 5 Ainv, 6 ldinv, 7 stream.
+ */
+int trsm_trtri_lower(trsm_dtype_t dtype, int64_t m, const void *A, int64_t lda,
+                     void *Ainv, int64_t ldinv, void *stream);
+
+/*
  * Size in bytes of the device array trsm_llnn_noalloc uses as its workspace
  * (32 MiB; every GPU that loads the library holds it until the process
  * exits).

@@ -16,7 +16,8 @@ def lib():
 
 
 EXPECTED = {"trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
-            "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string"}
+            "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_trtri_lower",
+            "trsm_status_string"}
 
 
 def test_header_declares_the_boundary():
@@ -162,6 +163,19 @@ def test_host_entry_argument_errors_and_quick_returns(lib):
     assert f(0, 0, 0, 4, one, None, 1, 0, None, 1, 4, 2, None) == 0
     assert f(0, 0, 4, 0, one, None, 4, 0, None, 4, 0, 2, None) == 0
     assert f(0, 0, 4, 4, one, None, 4, 16, None, 4, 16, 0, None) == 0
+
+
+def test_trtri_argument_errors_and_quick_return(lib):
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    f = lib.trsm_trtri_lower
+    assert f(9, 4, fake, 4, fake, 4, None) == -1
+    assert f(0, -1, fake, 4, fake, 4, None) == -2
+    assert f(0, 4, None, 4, fake, 4, None) == -3
+    assert f(1, 4, fake + 4, 4, fake, 4, None) == -3   # misaligned double
+    assert f(0, 4, fake, 3, fake, 4, None) == -4
+    assert f(0, 4, fake, 4, None, 4, None) == -5
+    assert f(0, 4, fake, 4, fake, 3, None) == -6
+    assert f(0, 0, None, 1, None, 1, None) == 0
 
 
 def test_small_regime_rejects_too_many_columns(lib):

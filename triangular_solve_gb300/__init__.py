@@ -74,10 +74,11 @@ def load_library():
         lib.trsm_llnn_ex.argtypes = [i32, i64, i64, vp, vp, i64, vp, i64, i64, vp, ctypes.c_size_t, vp]
         lib.trsm_llnn_profile.argtypes = [i32, i64, i64, vp, vp, i64, vp, i64, i64, vp, ctypes.c_size_t,
                                           vp, ctypes.POINTER(ctypes.c_float)]
+        lib.trsm_trtri_lower.argtypes = [i32, i64, vp, i64, vp, i64, vp]
         lib.trsm_status_string.argtypes = [i32]
         lib.trsm_status_string.restype = ctypes.c_char_p
         for name in ("trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
-                     "trsm_llnn_ex", "trsm_llnn_profile"):
+                     "trsm_llnn_ex", "trsm_llnn_profile", "trsm_trtri_lower"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -150,6 +151,13 @@ def trsm_llnn(dtype, m, n, alpha, A, lda, B, ldb, stream=None) -> None:
     al, _ = _alpha_buf(code, alpha)
     _check("trsm_llnn", load_library().trsm_llnn(code, m, n, al, _ptr(A), lda, _ptr(B), ldb,
                                                  _stream(stream)))
+
+
+def trsm_trtri_lower(dtype, m, A, lda, Ainv, ldinv, stream=None) -> None:
+    """Ainv = inverse of the lower triangle of A, both column-major; the
+    strictly upper part of Ainv is set to zero (see include/trsm.h)."""
+    _check("trsm_trtri_lower", load_library().trsm_trtri_lower(_dtype_code(dtype), m, _ptr(A), lda, _ptr(Ainv),
+                                                               ldinv, _stream(stream)))
 
 
 def trsm_llnn_strided_batched(dtype, layout, m, n, alpha, A, lda, strideA, B, ldb, strideB, batch,

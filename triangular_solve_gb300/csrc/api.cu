@@ -199,6 +199,26 @@ int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void 
     }
 }
 
+// Ainv <- I (m x m, column-major, ld): one thread per element of a column.
+template <typename T>
+__global__ void set_identity_kernel(T *__restrict__ D, int64_t m, int64_t ld) {
+    const int64_t j = blockIdx.y;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < m; i += (int64_t)gridDim.x * blockDim.x) {
+        D[j * ld + i] = (i == j) ? one_of<T>() : zero_of<T>();
+    }
+}
+
+int launch_set_identity(int dtype, void *D, int64_t m, int64_t ld, cudaStream_t st) {
+    const dim3 grid((unsigned)((m + 255) / 256 < 64 ? (m + 255) / 256 : 64), (unsigned)m);
+    switch (dtype) {
+        case TRSM_F32: set_identity_kernel<float><<<grid, 256, 0, st>>>(static_cast<float *>(D), m, ld); break;
+        case TRSM_F64: set_identity_kernel<double><<<grid, 256, 0, st>>>(static_cast<double *>(D), m, ld); break;
+        case TRSM_C64: set_identity_kernel<float2><<<grid, 256, 0, st>>>(static_cast<float2 *>(D), m, ld); break;
+        default: set_identity_kernel<double2><<<grid, 256, 0, st>>>(static_cast<double2 *>(D), m, ld); break;
+    }
+    return launch_status();
+}
+
 }  // namespace trsm
 
 extern "C" {
@@ -301,6 +321,31 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
         if (e != cudaSuccess) return cuda_status(e);
     }
     return rc;
+}
+
+int trsm_trtri_lower(trsm_dtype_t dtype, int64_t m, const void *A, int64_t lda, void *Ainv, int64_t ldinv,
+                     void *stream) {
+    const int eb = elem_bytes(dtype);
+    if (!eb) return -1;
+    if (m < 0) return -2;
+    if (lda < max1(m)) return -4;
+    if (ldinv < max1(m)) return -6;
+    if (m == 0) return TRSM_SUCCESS;
+    if (!A || !aligned(A, eb)) return -3;
+    if (!Ainv || !aligned(Ainv, eb)) return -5;
+    if (m > 65535) return -2;  // one grid row per column of the identity
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = launch_set_identity((int)dtype, Ainv, m, ldinv, st);
+    if (rc) return rc;
+    alignas(16) unsigned char one[16] = {};
+    if (dtype == TRSM_F32 || dtype == TRSM_C64) {
+        const float f = 1.f;
+        memcpy(one, &f, sizeof f);
+    } else {
+        const double d = 1.0;
+        memcpy(one, &d, sizeof d);
+    }
+    return solve(dtype, TRSM_COL_MAJOR, m, m, one, A, lda, 0, Ainv, ldinv, 0, 1, 0, nullptr, 0, true, st, nullptr);
 }
 
 int trsm_device_status(int clear) { return device_status(clear); }
