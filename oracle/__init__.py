@@ -1,4 +1,6 @@
-"""CPU oracle for the left-lower, non-transposed, non-unit TRSM  L X = alpha B.
+"""CPU oracle for the left-lower, non-transposed, non-unit TRSM  L X = alpha B,
+and for every other TRSM variant (``trsm_general``: side, triangle, op, unit
+diagonal; BLAS meaning).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
@@ -13,7 +15,11 @@ Parity status: pinned.  ``tests/test_oracle_pins.py`` checks it against the
 identity and diagonal special cases, exact integer recovery, the bidiagonal
 and all-ones closed forms, brute-force Gaussian elimination with partial
 pivoting on m <= 8, LAPACK's triangular solve, and the backward-error bound
-on every workload's inputs.
+on every workload's inputs.  ``tests/test_oracle_variants.py`` pins the
+general variants: a dense library solve of the explicitly formed op(A) for
+all 24 variants and four types (NaN in every entry a variant must not read),
+bitwise agreement with the left-lower oracle, bidiagonal suffix-sum closed
+forms for the left-upper and right-lower cases, and alpha = 0.
 """
 from __future__ import annotations
 
@@ -62,6 +68,10 @@ def _load():
                 ctypes.c_int]
             lib.oracle_trsm_llnn.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
+            ci = ctypes.c_int
+            lib.oracle_trsm_general.argtypes = [ci, ci, ci, ci, ci, i64, i64, ctypes.POINTER(ctypes.c_double),
+                                                vp, i64, vp, i64]
+            lib.oracle_trsm_general.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -99,3 +109,28 @@ def trsm_llnn(dtype: str, m: int, n: int, alpha, A: np.ndarray, lda: int, B: np.
         B.ctypes.data, int(ldb), int(stride_b), int(batch), cp, nc, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_trsm_llnn: invalid argument {-rc}")
+
+
+SIDES = {"L": 0, "R": 1}
+UPLOS = {"L": 0, "U": 1}
+OPS = {"N": 0, "T": 1, "C": 2}
+DIAGS = {"N": 0, "U": 1}
+
+
+def trsm_general(dtype: str, side: str, uplo: str, trans: str, diag: str, m: int, n: int, alpha,
+                 A: np.ndarray, lda: int, B: np.ndarray, ldb: int) -> None:
+    """Any TRSM variant (BLAS meaning: side L/R, uplo L/U, trans N/T/C, diag
+    N/U), column-major, one system, in place in ``B``; see
+    ``oracle_trsm_general`` in ``trsm_oracle.c``."""
+    np_t = NUMPY[dtype]
+    if B.dtype != np_t or (A is not None and A.dtype != np_t):
+        raise TypeError(f"oracle: arrays must be {np_t}")
+    if not B.flags.c_contiguous or (A is not None and not A.flags.c_contiguous):
+        raise ValueError("oracle: arrays must be C-contiguous buffers")
+    a = complex(alpha)
+    al = (ctypes.c_double * 2)(a.real, a.imag)
+    rc = _load().oracle_trsm_general(DTYPES[dtype], SIDES[side], UPLOS[uplo], OPS[trans], DIAGS[diag],
+                                     int(m), int(n), al, None if A is None else A.ctypes.data, int(lda),
+                                     B.ctypes.data, int(ldb))
+    if rc != 0:
+        raise ValueError(f"oracle_trsm_general: invalid argument {-rc}")

@@ -1,6 +1,8 @@
 /*
  * Oracle for the left-side, lower-triangular, non-transposed, non-unit-diagonal
- * triangular solve  L * X = alpha * B  (X overwrites B).
+ * triangular solve  L * X = alpha * B  (X overwrites B), and, in
+ * oracle_trsm_general, for every other TRSM variant (side, triangle,
+ * transpose / conjugate transpose, unit diagonal) from its BLAS definition.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may build, load or call this file.  It shares
@@ -236,6 +238,97 @@ int oracle_trsm_llnn(int dtype, int layout, int64_t m, int64_t n, const double *
         free(s);
     }
     (void)nthreads;
+    return 0;
+}
+
+/*
+ * Every TRSM variant, from its BLAS definition (the pages call the variants
+ * beyond left/lower/no-transpose "other TRSM variants"; their meaning is the
+ * standard xTRSM one):
+ *   side 0 (left):   op(A) X = alpha B,  A is m x m
+ *   side 1 (right):  X op(A) = alpha B,  A is n x n
+ *   op(A) = A (trans 0), A^T (1) or A^H (2; A^T for real types); only the
+ *   triangle `uplo` (0 lower, 1 upper) of A is read; diag 1 (unit) takes the
+ *   diagonal as 1 without reading it.  Column-major, one system, serial.
+ * The triangular matrix T = op(A) is read entry by entry through t_entry();
+ * the substitution runs in the order T's shape dictates: for the left side
+ * forward (T lower) or backward (T upper) over the rows of X, for the right
+ * side forward (T upper) or backward (T lower) over its columns, each x
+ * being (alpha b - the sum of the already solved terms, in the order they
+ * were solved) / T_jj.  Double precision throughout, one rounding at the end.
+ * Returns 0, or -k when argument k is invalid.
+ */
+static ocplx t_entry(int dtype, int uplo, int trans, int diag, const void *A, int64_t lda, int64_t i,
+                     int64_t j) {
+    ocplx v = {0.0, 0.0};
+    if (i == j && diag == 1) {
+        v.re = 1.0;
+        return v;
+    }
+    /* T(i, j) = A(i, j), A(j, i) or conj(A(j, i)) */
+    const int64_t r = trans ? j : i, c = trans ? i : j;
+    if ((uplo == 0 && r < c) || (uplo == 1 && r > c)) return v; /* outside the referenced triangle */
+    if (dtype >= OR_C64) {
+        v = ld_cplx(A, dtype, c * lda + r);
+        if (trans == 2) v.im = -v.im;
+    } else {
+        v.re = ld_real(A, dtype, c * lda + r);
+    }
+    return v;
+}
+
+int oracle_trsm_general(int dtype, int side, int uplo, int trans, int diag, int64_t m, int64_t n,
+                        const double *alpha, const void *A, int64_t lda, void *B, int64_t ldb) {
+    if (dtype < 0 || dtype > 3) return -1;
+    if (side != 0 && side != 1) return -2;
+    if (uplo != 0 && uplo != 1) return -3;
+    if (trans < 0 || trans > 2) return -4;
+    if (diag != 0 && diag != 1) return -5;
+    if (m < 0) return -6;
+    if (n < 0) return -7;
+    if (!alpha) return -8;
+    const int64_t k = side == 0 ? m : n;
+    if (lda < (k > 1 ? k : 1)) return -10;
+    if (ldb < (m > 1 ? m : 1)) return -12;
+    if (m == 0 || n == 0) return 0;
+    if (!B) return -11;
+    const int cplx = dtype >= OR_C64;
+    const int zero_alpha = alpha[0] == 0.0 && (!cplx || alpha[1] == 0.0);
+    if (!zero_alpha && !A) return -9;
+    const ocplx al = {alpha[0], cplx ? alpha[1] : 0.0};
+    /* T lower when the referenced triangle is lower and not transposed, or upper and transposed */
+    const int t_lower = (uplo == 0) != (trans != 0);
+    ocplx *x = (ocplx *)malloc((size_t)k * sizeof(ocplx));
+    const int64_t systems = side == 0 ? n : m; /* columns (left) or rows (right) of X */
+    for (int64_t s = 0; s < systems; ++s) {
+        /* the vector being solved: column s of B (left) or row s of B (right) */
+        for (int64_t q = 0; q < k; ++q) {
+            const int64_t o = side == 0 ? s * ldb + q : q * ldb + s;
+            ocplx b = cplx ? ld_cplx(B, dtype, o) : (ocplx){ld_real(B, dtype, o), 0.0};
+            x[q] = zero_alpha ? (ocplx){0.0, 0.0} : c_mul(al, b);
+        }
+        if (!zero_alpha) {
+            /* left: T x = rhs (x a column); right: x T = rhs, i.e. T^T x = rhs */
+            const int lower_system = side == 0 ? t_lower : !t_lower;
+            for (int64_t step = 0; step < k; ++step) {
+                const int64_t j = lower_system ? step : k - 1 - step;
+                ocplx acc = x[j];
+                for (int64_t st = 0; st < step; ++st) {
+                    const int64_t q = lower_system ? st : k - 1 - st;
+                    const ocplx tv = side == 0 ? t_entry(dtype, uplo, trans, diag, A, lda, j, q)
+                                               : t_entry(dtype, uplo, trans, diag, A, lda, q, j);
+                    acc = c_sub(acc, c_mul(tv, x[q]));
+                }
+                x[j] = c_div(acc, t_entry(dtype, uplo, trans, diag, A, lda, j, j));
+            }
+        }
+        for (int64_t q = 0; q < k; ++q) {
+            const int64_t o = side == 0 ? s * ldb + q : q * ldb + s;
+            if (cplx) st_cplx(B, dtype, o, x[q]);
+            else st_real(B, dtype, o, x[q].re);
+        }
+    }
+    free(x);
     return 0;
 }
 

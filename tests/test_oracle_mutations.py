@@ -32,6 +32,37 @@ MUTANTS = [
 ]
 
 
+# mistakes in the general-variant solve, caught by tests/test_oracle_variants.py
+VARIANT_MUTANTS = [
+    ("if (trans == 2) v.im = -v.im;", "if (trans == 1) v.im = -v.im;"),          # conjugates the wrong op
+    ("const int64_t r = trans ? j : i, c = trans ? i : j;",
+     "const int64_t r = i, c = j;"),                                               # transpose dropped
+    ("const int lower_system = side == 0 ? t_lower : !t_lower;",
+     "const int lower_system = t_lower;"),                                          # right side solved as left
+    ("if (i == j && diag == 1) {", "if (i == j && diag == 2) {"),                 # unit diagonal ignored
+    ("acc = c_sub(acc, c_mul(tv, x[q]));", "acc = c_sub(acc, c_mul(tv, x[j]));"),  # wrong index
+]
+
+
+def _run_pins_on_mutant(tmp_path, before, after, pin_file):
+    src = open(SRC).read()
+    assert before in src, "mutation anchor no longer in the oracle source"
+    mutant = tmp_path / "trsm_oracle.c"
+    mutant.write_text(src.replace(before, after, 1))
+    env = dict(os.environ, TRSM_ORACLE_TEST_SRC=str(mutant),
+               TRSM_ORACLE_TEST_BUILD=str(tmp_path / "build"))
+    return subprocess.run(
+        [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+         os.path.join(ROOT, "tests", pin_file)],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+@pytest.mark.parametrize("idx", range(len(VARIANT_MUTANTS)))
+def test_variant_pins_reject_planted_mistake(tmp_path, idx):
+    r = _run_pins_on_mutant(tmp_path, *VARIANT_MUTANTS[idx], "test_oracle_variants.py")
+    assert r.returncode == 1 and "failed" in r.stdout, r.stdout[-2000:]
+
+
 @pytest.mark.parametrize("idx", range(len(MUTANTS)))
 def test_pins_reject_planted_mistake(tmp_path, idx):
     before, after = MUTANTS[idx]
