@@ -425,6 +425,59 @@ def run_large(torch, tg, dev, stream, peaks, reps=2):
     return res
 
 
+def variants_bench(args):
+    """One JSON line per (type, m, variant): trsm_general on a square system
+    (m = n; side, triangle, op, diagonal as in BLAS), CUDA events on the
+    launching stream, inputs resident, B restored before every run; GFLOPS
+    credit m^2 n (x4 complex) and `vs_llnn` is the native left-lower time
+    over this variant's (the mapped variants add the copies of A and B)."""
+    import itertools
+
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    for d in args.sweep_dtypes.split(","):
+        for mm in [int(x) for x in args.sweep_ms.split(",")]:
+            rng = np.random.default_rng(0)
+            cplx = d in ("c64", "c128")
+
+            def u(shape):
+                x = rng.uniform(-1, 1, shape)
+                return x + 1j * rng.uniform(-1, 1, shape) if cplx else x
+
+            A = u((mm, mm)) / mm
+            A[np.diag_indices(mm)] = 1 + rng.uniform(0, 1, mm)
+            a = torch.from_numpy(ti.to_storage(A.astype(ti.NUMPY[d])[None], "col")).to(dev)
+            b0 = torch.from_numpy(ti.to_storage(u((mm, mm)).astype(ti.NUMPY[d])[None], "col")).to(dev)
+            del A
+            b = torch.empty_like(b0)
+            base = None
+            for v in ["LLNN"] + ["".join(x) for x in itertools.product("LR", "LU", "NTC", "NU")
+                                 if "".join(x) != "LLNN"]:
+                b.copy_(b0)
+                tg.trsm_general(d, v[0], v[1], v[2], v[3], mm, mm, 1.0, a, mm, b, mm, stream)  # warm-up
+                times = []
+                for _ in range(max(args.sweep_reps, 1)):
+                    b.copy_(b0)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    tg.trsm_general(d, v[0], v[1], v[2], v[3], mm, mm, 1.0, a, mm, b, mm, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                ms = statistics.mean(times)
+                base = ms if base is None else base
+                print(json.dumps({"op": "trsm_general", "dtype": d, "m": mm, "n": mm, "variant": v,
+                                  "ms": round(ms, 3), "gflops": round(ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9, 1),
+                                  "vs_llnn": round(base / ms, 3)}), flush=True)
+            del a, b0, b
+            torch.cuda.empty_cache()
+
+
 def trtri_bench(args):
     """One JSON line per (type, m): the triangular inverse L^-1 through
     trsm_trtri_lower (set to I, then the L X = I solve), CUDA events on the
@@ -637,6 +690,8 @@ def main():
     ap.add_argument("--dtypes", default="f32,f64,c64,c128",
                     help="subset of the step's types (profiling a single kernel)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--variants", action="store_true",
+                    help="time every TRSM variant (trsm_general) at m = n = --sweep-ms per --sweep-dtypes")
     ap.add_argument("--trtri", action="store_true",
                     help="time the exported triangular inverse (trsm_trtri_lower) at --sweep-ms per --sweep-dtypes")
     args = ap.parse_args()
@@ -655,6 +710,9 @@ def main():
         return
     if args.trtri:
         trtri_bench(args)
+        return
+    if args.variants:
+        variants_bench(args)
         return
     run_gb300(args, ws, rank, local)
 

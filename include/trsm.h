@@ -54,6 +54,11 @@ extern "C" {
 
 typedef enum { TRSM_F32 = 0, TRSM_F64 = 1, TRSM_C64 = 2, TRSM_C128 = 3 } trsm_dtype_t;
 typedef enum { TRSM_COL_MAJOR = 0, TRSM_ROW_MAJOR = 1 } trsm_layout_t;
+/* the other TRSM variants (trsm_general) */
+typedef enum { TRSM_LEFT = 0, TRSM_RIGHT = 1 } trsm_side_t;
+typedef enum { TRSM_LOWER = 0, TRSM_UPPER = 1 } trsm_uplo_t;
+typedef enum { TRSM_NOTRANS = 0, TRSM_TRANS = 1, TRSM_CONJTRANS = 2 } trsm_op_t;
+typedef enum { TRSM_NONUNIT = 0, TRSM_UNIT = 1 } trsm_diag_t;
 
 #define TRSM_SUCCESS 0
 #define TRSM_ERR_WORKSPACE 900      /* caller workspace too small or misaligned */
@@ -168,6 +173,34 @@ int trsm_llnn_ex(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
 int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
                       const void *A, int64_t lda, void *B, int64_t ldb, int64_t nb,
                       void *workspace, size_t ws_bytes, void *stream, float *ms);
+
+/*
+ * Every TRSM variant, with the BLAS xTRSM meaning ("Hierarchical Shared
+ * Memory-Aware Optimization for TRSM on GPU Platforms" leaves the variants
+ * beyond the left / lower / no-transpose case open):
+ *   side TRSM_LEFT:   op(A) X = alpha B,  A is m x m (lda >= max(1,m))
+ *   side TRSM_RIGHT:  X op(A) = alpha B,  A is n x n (lda >= max(1,n))
+ * with op(A) = A, A^T or A^H (TRSM_CONJTRANS; the same as A^T for real
+ * types), only the triangle `uplo` of A read, and for TRSM_UNIT the diagonal
+ * taken as 1 and never read.  B is m x n, column-major (ldb >= max(1,m)), and
+ * is overwritten with X.
+ *
+ * The left / lower / no-transpose / non-unit case is trsm_llnn itself.  Any
+ * other is mapped onto it: the matrix of the equivalent left-side lower
+ * problem (op(A), or op(A)^T for the right side, reversed in row and column
+ * order when it is upper, with the unit diagonal written in) is copied into
+ * a stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`,
+ * k^2 elements, plus m n for the right side), B is reversed in row order or
+ * transposed into the workspace around the solve, and trsm_llnn runs on it.
+ * alpha = 0 sets B to zero without reading A.  The order of A and the other
+ * dimension are limited to 65535 for the variants that copy.
+ *
+ * Arguments: 1 dtype, 2 side, 3 uplo, 4 trans, 5 diag, 6 m, 7 n, 8 alpha,
+ * 9 A, 10 lda, 11 B, 12 ldb, 13 stream.
+ */
+int trsm_general(trsm_dtype_t dtype, trsm_side_t side, trsm_uplo_t uplo, trsm_op_t trans,
+                 trsm_diag_t diag, int64_t m, int64_t n, const void *alpha,
+                 const void *A, int64_t lda, void *B, int64_t ldb, void *stream);
 
 /*
  * Triangular inverse (TRTRI, lower, non-unit):  Ainv = L^{-1}, the inverse

@@ -17,7 +17,7 @@ def lib():
 
 EXPECTED = {"trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
             "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_trtri_lower",
-            "trsm_status_string"}
+            "trsm_general", "trsm_status_string"}
 
 
 def test_header_declares_the_boundary():
@@ -176,6 +176,26 @@ def test_trtri_argument_errors_and_quick_return(lib):
     assert f(0, 4, fake, 4, None, 4, None) == -5
     assert f(0, 4, fake, 4, fake, 3, None) == -6
     assert f(0, 0, None, 1, None, 1, None) == 0
+
+
+def test_general_variant_argument_errors_and_quick_returns(lib):
+    one = ctypes.byref(ctypes.c_double(1.0))
+    fake = 1 << 20  # never dereferenced: every call below fails validation or returns first
+    f = lib.trsm_general
+    assert f(7, 0, 0, 0, 0, 4, 4, one, fake, 4, fake, 4, None) == -1
+    assert f(1, 2, 0, 0, 0, 4, 4, one, fake, 4, fake, 4, None) == -2
+    assert f(1, 0, 2, 0, 0, 4, 4, one, fake, 4, fake, 4, None) == -3
+    assert f(1, 0, 0, 3, 0, 4, 4, one, fake, 4, fake, 4, None) == -4
+    assert f(1, 0, 0, 0, 2, 4, 4, one, fake, 4, fake, 4, None) == -5
+    assert f(1, 0, 0, 0, 0, -1, 4, one, fake, 4, fake, 4, None) == -6
+    assert f(1, 0, 0, 0, 0, 4, -1, one, fake, 4, fake, 4, None) == -7
+    assert f(1, 0, 0, 0, 0, 4, 4, None, fake, 4, fake, 4, None) == -8
+    assert f(1, 1, 1, 1, 1, 4, 6, one, None, 6, fake, 4, None) == -9
+    assert f(1, 1, 0, 0, 0, 4, 6, one, fake, 5, fake, 4, None) == -10   # right side: lda >= n
+    assert f(1, 0, 1, 0, 0, 4, 6, one, fake, 4, None, 4, None) == -11
+    assert f(1, 0, 1, 0, 0, 4, 6, one, fake, 4, fake, 3, None) == -12
+    assert f(1, 1, 1, 2, 1, 0, 6, one, None, 6, None, 1, None) == 0
+    assert f(1, 1, 1, 2, 1, 4, 0, one, None, 1, None, 4, None) == 0
 
 
 def test_small_regime_rejects_too_many_columns(lib):

@@ -75,10 +75,11 @@ def load_library():
         lib.trsm_llnn_profile.argtypes = [i32, i64, i64, vp, vp, i64, vp, i64, i64, vp, ctypes.c_size_t,
                                           vp, ctypes.POINTER(ctypes.c_float)]
         lib.trsm_trtri_lower.argtypes = [i32, i64, vp, i64, vp, i64, vp]
+        lib.trsm_general.argtypes = [i32, i32, i32, i32, i32, i64, i64, vp, vp, i64, vp, i64, vp]
         lib.trsm_status_string.argtypes = [i32]
         lib.trsm_status_string.restype = ctypes.c_char_p
         for name in ("trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
-                     "trsm_llnn_ex", "trsm_llnn_profile", "trsm_trtri_lower"):
+                     "trsm_llnn_ex", "trsm_llnn_profile", "trsm_trtri_lower", "trsm_general"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -151,6 +152,31 @@ def trsm_llnn(dtype, m, n, alpha, A, lda, B, ldb, stream=None) -> None:
     al, _ = _alpha_buf(code, alpha)
     _check("trsm_llnn", load_library().trsm_llnn(code, m, n, al, _ptr(A), lda, _ptr(B), ldb,
                                                  _stream(stream)))
+
+
+_SIDE = {"L": 0, "R": 1}
+_UPLO = {"L": 0, "U": 1}
+_OP = {"N": 0, "T": 1, "C": 2}
+_DIAG = {"N": 0, "U": 1}
+
+
+def _flag(table, v, what):
+    if isinstance(v, str) and v.upper() in table:
+        return table[v.upper()]
+    if isinstance(v, int) and v in table.values():
+        return v
+    raise ValueError(f"{what}: {v!r}")
+
+
+def trsm_general(dtype, side, uplo, trans, diag, m, n, alpha, A, lda, B, ldb, stream=None) -> None:
+    """Any TRSM variant, BLAS meaning (side "L"/"R", uplo "L"/"U", trans
+    "N"/"T"/"C", diag "N"/"U"), column-major, in place in B (see
+    include/trsm.h)."""
+    code = _dtype_code(dtype)
+    al, _ = _alpha_buf(code, alpha)
+    _check("trsm_general", load_library().trsm_general(
+        code, _flag(_SIDE, side, "side"), _flag(_UPLO, uplo, "uplo"), _flag(_OP, trans, "trans"),
+        _flag(_DIAG, diag, "diag"), m, n, al, _ptr(A), lda, _ptr(B), ldb, _stream(stream)))
 
 
 def trsm_trtri_lower(dtype, m, A, lda, Ainv, ldinv, stream=None) -> None:
