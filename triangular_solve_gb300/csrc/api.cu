@@ -59,6 +59,8 @@ int nearest_nb(int dtype, int64_t m) {
     return best ? best : 256;
 }
 
+constexpr int kFastNotApplicableCode = -100000;  // launch_fast_*: preconditions not met
+
 int launch_small(int dtype, const SmallArgs &a, cudaStream_t st) {
     if (a.n <= 8) {
         switch (dtype) {
@@ -126,6 +128,33 @@ int solve(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const 
             cudaEventDestroy(e1);
         }
         return rc;
+    }
+
+    if (m == 128 && layout == TRSM_COL_MAJOR && n > 8) {
+        // a medium system fits on chip: the whole batch in one launch of the
+        // small regime's chunked kernel instead of the blocked path system by
+        // system (falls through when its alignment preconditions fail)
+        cudaEvent_t e0 = nullptr, e1 = nullptr;
+        if (ms) {
+            cudaEventCreate(&e0);
+            cudaEventCreate(&e1);
+            cudaEventRecord(e0, st);
+        }
+        int rc = kFastNotApplicableCode;
+        switch (dtype) {
+            case TRSM_F32: rc = launch_fast_f32(s, st); break;
+            case TRSM_F64: rc = launch_fast_f64(s, st); break;
+            case TRSM_C64: rc = launch_fast_c64(s, st); break;
+            default: rc = launch_fast_c128(s, st); break;
+        }
+        if (ms) {
+            cudaEventRecord(e1, st);
+            cudaEventSynchronize(e1);
+            if (rc != kFastNotApplicableCode) cudaEventElapsedTime(&ms[1], e0, e1);
+            cudaEventDestroy(e0);
+            cudaEventDestroy(e1);
+        }
+        if (rc != kFastNotApplicableCode) return rc;
     }
 
     const int eb = elem_bytes(dtype);

@@ -34,8 +34,8 @@ int launch_rowlane_c64(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st);
 
 // Fast path of the thread-per-column kernel for aligned full-size systems
-// (m in {8, 16, 32, 48, 64}); returns kFastNotApplicable (-100000) when its
-// preconditions do not hold.
+// (m in {8, 16, 32, 48, 64}, and 128 for batches of medium systems); returns
+// kFastNotApplicable (-100000) when its preconditions do not hold.
 int launch_fast_f32(const SmallArgs &a, cudaStream_t st);
 int launch_fast_f64(const SmallArgs &a, cudaStream_t st);
 int launch_fast_c64(const SmallArgs &a, cudaStream_t st);

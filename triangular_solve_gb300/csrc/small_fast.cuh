@@ -913,6 +913,18 @@ static int launch_fast_m(const SmallGeom &g, T alpha, cudaStream_t st) {
     return launch_fast_mw<T, M, 64, CPT, RC>(g, alpha, st);
 }
 
+// m = 128 (batches of medium systems, which otherwise run one by one through
+// the blocked path): the chunked kernel alone -- 32-row chunks for the real
+// types, 16 for the complex ones, one CTA holding up to three f32 systems or
+// one system of the other types (L packed in shared memory: 66-132 KB).
+template <typename T>
+static int launch_fast_128(const SmallGeom &g, T alpha, cudaStream_t st) {
+    constexpr int CPT = std::is_same<T, float>::value ? 2 : 1;
+    constexpr int RC = Elem<T>::kComplex ? 16 : 32;
+    if (g.n <= 32) return launch_fast_mw<T, 128, 32, CPT, RC>(g, alpha, st);
+    return launch_fast_mw<T, 128, 64, CPT, RC>(g, alpha, st);
+}
+
 // The fast kernel's preconditions: column-major, m one of the compiled
 // sizes, every column and system start 16-byte aligned.  Returns
 // kFastNotApplicable otherwise (the general kernel then runs).
@@ -936,6 +948,7 @@ int launch_fast_typed(const SmallArgs &a, cudaStream_t st) {
         case 32: return launch_fast_m<T, 32>(g, alpha, st);
         case 48: return launch_fast_m<T, 48>(g, alpha, st);
         case 64: return launch_fast_m<T, 64>(g, alpha, st);
+        case 128: return launch_fast_128<T>(g, alpha, st);
         default: return kFastNotApplicable;
     }
 }

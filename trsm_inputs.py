@@ -126,7 +126,9 @@ def to_storage(X: np.ndarray, layout: str = "col", ld: int | None = None,
     if batch > 1 and stride < major * ld:
         raise ValueError("batch stride too small")
     fill = np.nan if pad is None else pad
-    buf = np.full(max(batch * stride, 1), fill, dtype=X.dtype)
+    # every system's extent: (batch-1)*stride + major*ld (stride 0: one matrix shared by the batch)
+    size = max(batch * stride, (batch - 1) * stride + major * ld, 1)
+    buf = np.full(size, fill, dtype=X.dtype)
     if batch * major * minor:
         view = np.lib.stride_tricks.as_strided(
             buf, shape=(batch, major, minor),
