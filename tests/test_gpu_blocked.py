@@ -152,6 +152,28 @@ def test_tensor_core_products_ragged(env, dtype, nb, m, n):
     assert_parity(dtype, xg, xr, f"tc {dtype} m={m} n={n} nb={nb}")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("m,n", [(65, 1), (129, 3), (300, 8), (1000, 2), (4096, 1)])
+def test_narrow_path(env, dtype, m, n):
+    """Few right-hand sides (n <= 8) through the blocked path: short last
+    blocks, every type, padded leading dimensions."""
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + 17 * n)
+    alpha = (1.5 - 0.5j) if ti.IS_COMPLEX[dtype] else 1.5
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, 0, lda=m + 3, ldb=m + 1)
+    assert env["tg"].trsm_device_status() == 0
+    assert_parity(dtype, xg, xr, f"narrow {dtype} m={m} n={n}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_narrow_path_large(env, dtype):
+    """m = 16384, n = 1: a single right-hand side at full size."""
+    m = 16384
+    L, B = ti.generate(dtype, m, 1, 1, kind="ddm")
+    xg, xr = _ex_solve(env, dtype, L, B, 1.0, 0)
+    assert env["tg"].trsm_device_status() == 0
+    assert_parity(dtype, xg, xr, f"narrow {dtype} m={m}")
+
+
 @pytest.mark.parametrize("m,n,nb,ld_pad", [
     (512, 256, 256, 0),    # two blocks: one update, then both applies in one launch
     (528, 257, 256, 1),    # 16-row last block, one column past a tile, odd ldb (scalar splits)
