@@ -169,29 +169,62 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- helpers
-def kernel_source_hash():
-    """Hash of the CUDA sources: ncu traffic figures are only valid for the
-    kernels they were captured on."""
-    h = hashlib.sha256()
+def source_closure(tu):
+    """A CUDA translation unit under csrc/ and every file it includes with
+    quotes, transitively (resolved beside the including file, in csrc/ or in
+    include/)."""
+    import re
     csrc = os.path.join(ROOT, "triangular_solve_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
+    inc = os.path.join(ROOT, "include")
+    seen, stack = [], [os.path.join(csrc, tu)]
+    while stack:
+        p = os.path.normpath(stack.pop())
+        if p in seen or not os.path.exists(p):
+            continue
+        seen.append(p)
+        with open(p) as f:
+            for line in f:
+                mm = re.match(r'\s*#include\s+"([^"]+)"', line)
+                if not mm:
+                    continue
+                for base in (os.path.dirname(p), csrc, inc):
+                    q = os.path.join(base, mm.group(1))
+                    if os.path.exists(q):
+                        stack.append(q)
+                        break
+    return sorted(seen)
+
+
+def kernel_source_hash(tu=None):
+    """Hash of the sources a kernel is built from (its translation unit's
+    include closure; all CUDA sources when none is named): ncu traffic
+    figures are only valid for the kernels they were captured on."""
+    h = hashlib.sha256()
+    if tu is None:
+        csrc = os.path.join(ROOT, "triangular_solve_gb300", "csrc")
+        files = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh", ".h"))]
+        for p in files:
+            with open(p, "rb") as f:
+                h.update(os.path.basename(p).encode())
                 h.update(f.read())
+        return h.hexdigest()[:16]
+    for p in source_closure(tu):
+        with open(p, "rb") as f:
+            h.update(os.path.relpath(p, ROOT).encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_key):
     """dram bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since the capture."""
+    kernel's sources changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel_key)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(e.get("translation_unit")):
         return None
     return e.get("dram_bytes_per_launch")
 

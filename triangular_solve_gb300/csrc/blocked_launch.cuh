@@ -6,6 +6,7 @@
 #include "blocked_kernels.cuh"
 #include "gemm_sp.cuh"
 #include "internal.h"
+#include "tc_side.h"
 
 namespace trsm {
 
@@ -228,9 +229,12 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
             // update with the previous block's apply folded in (phase 2);
             // the last holds the two remaining applies (phase 1)
             timer.begin();
-            rc = tc_fused_prepare(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st);
+            TcSide side;
+            rc = tc_side_open(side, st);
+            if (!rc) rc = tc_fused_prepare_side(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, &side);
             for (int64_t t = 0; !rc && t + 1 < tb; ++t)
-                rc = tc_fused_step(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+                rc = tc_fused_step_side(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, &side);
+            tc_side_close(side);
             if (rc || (rc = timer.end(2))) return rc;
             timer.begin();
             rc = tc_fused_step(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);

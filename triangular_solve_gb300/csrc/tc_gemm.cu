@@ -9,6 +9,7 @@
 
 #include "internal.h"
 #include "tc_gemm.cuh"
+#include "tc_side.h"
 
 namespace trsm {
 
@@ -410,10 +411,12 @@ int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, 
 //
 // Workspace (256-byte aligned regions, rows padded for the TMA boxes):
 //   wp[2]   W_t head/tail, RA x nb (A operand of the update; double buffer)
-//   lp      L_panel_{t+1} head/tail, RA x nb (X operand of W_{t+1}^T)
+//   lp[2]   L_panel_b head/tail, RA x nb (X operand of W_b^T; double buffer:
+//           block b's copy is made on a side stream while launch b-2 runs)
 //   xs[3]   R_t head/tail, RX x nb (X operand of update t and apply t; launch
 //           t reads R_t and R_{t-1} and writes R_{t+1}: three buffers)
-//   d0, d1  D^-1 (apply) or D^-T (W product) rows, head/tail, nb x nb
+//   d0      D^-1 rows (apply), head/tail, nb x nb
+//   d1[2]   D_b^-T rows (W product; made with lp[b & 1]), head/tail, nb x nb
 // with RA = m and RX = n rounded up to 256 rows.
 // ---------------------------------------------------------------------------
 namespace {
@@ -423,7 +426,7 @@ namespace {
 constexpr int64_t kTcFusedMinN = 256;
 
 struct TcFused {
-    float *wp_hi[2], *wp_lo[2], *lp_hi, *lp_lo, *xs_hi[3], *xs_lo[3], *d0_hi, *d0_lo, *d1_hi, *d1_lo;
+    float *wp_hi[2], *wp_lo[2], *lp_hi[2], *lp_lo[2], *xs_hi[3], *xs_lo[3], *d0_hi, *d0_lo, *d1_hi[2], *d1_lo[2];
     int64_t ra, rx;
 };
 
@@ -444,27 +447,36 @@ TcFused tc_fused_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
         f.wp_hi[i] = take(A);
         f.wp_lo[i] = take(A);
     }
-    f.lp_hi = take(A);
-    f.lp_lo = take(A);
+    for (int i = 0; i < 2; ++i) {
+        f.lp_hi[i] = take(A);
+        f.lp_lo[i] = take(A);
+    }
     for (int i = 0; i < 3; ++i) {
         f.xs_hi[i] = take(X);
         f.xs_lo[i] = take(X);
     }
     f.d0_hi = take(D);
     f.d0_lo = take(D);
-    f.d1_hi = take(D);
-    f.d1_lo = take(D);
+    for (int i = 0; i < 2; ++i) {
+        f.d1_hi[i] = take(D);
+        f.d1_lo[i] = take(D);
+    }
     return f;
 }
 
-// The W_{t+1}^T product of launch t (and of the preparation, t = -1): block
-// b = t + 1, its L panel and D_b^-T split, then the problem emitting W_b.
-int tc_w_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t nb, const float *L, int64_t lda,
-                 const float *W, cudaStream_t st) {
+// The operands of block b's W product, which depend on L and D_b^-1 only:
+// its L panel and D_b^-T split into lp[b & 1], d1[b & 1].
+int tc_w_splits(const TcFused &f, int64_t b, int64_t m, int64_t nb, const float *L, int64_t lda, const float *W,
+                cudaStream_t st) {
     const int64_t r1 = b * nb, rows = m - r1 - nb;
-    int rc = split(L + r1 * lda + r1 + nb, lda, rows, nb, f.lp_hi, f.lp_lo, nb, st);  // L panel rows, K-major
-    if (!rc) rc = split_rows(W + b * nb * nb, nb, nb, nb, f.d1_hi, f.d1_lo, nb, st);  // rows of D_b^-T
-    if (rc) return rc;
+    const int rc = split(L + r1 * lda + r1 + nb, lda, rows, nb, f.lp_hi[b & 1], f.lp_lo[b & 1], nb, st);
+    return rc ? rc : split_rows(W + b * nb * nb, nb, nb, nb, f.d1_hi[b & 1], f.d1_lo[b & 1], nb, st);
+}
+
+// The W_{t+1}^T product of launch t (and of the preparation, t = -1): block
+// b = t + 1, from its split operands, emitting W_b.
+int tc_w_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t nb) {
+    const int64_t r1 = b * nb, rows = m - r1 - nb;
     TcArgs g = tc_args(nb, rows, nb, nullptr, 0);
     g.beta_zero = 1;
     g.gamma = 1.f;
@@ -472,7 +484,7 @@ int tc_w_problem(TcProblem &q, const TcFused &f, int64_t b, int64_t m, int64_t n
     g.xhi = f.wp_hi[b & 1];
     g.xlo = f.wp_lo[b & 1];
     g.ldxs = nb;
-    return tc_problem(q, f.d1_hi, f.d1_lo, nb, f.lp_hi, f.lp_lo, f.ra, nb, g);
+    return tc_problem(q, f.d1_hi[b & 1], f.d1_lo[b & 1], nb, f.lp_hi[b & 1], f.lp_lo[b & 1], f.ra, nb, g);
 }
 
 // The apply of block b over its block row (R_b split in xs[b % 3]); the D_b^-1
@@ -500,27 +512,72 @@ bool tc_fused_usable(int64_t m, int64_t n, int64_t nb) {
 
 size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb) {
     const int64_t ra = round_rows(m), rx = round_rows(n);
-    return (size_t)(6 * round256(ra * nb * 4) + 6 * round256(rx * nb * 4) + 4 * round256(nb * nb * 4));
+    return (size_t)(8 * round256(ra * nb * 4) + 6 * round256(rx * nb * 4) + 6 * round256(nb * nb * 4));
 }
 
-// W_0 = L_panel_0 D_0^-1 and the split of R_0, before step 0.
-int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
-                     int64_t ldb, void *panels, cudaStream_t st) {
+// The side stream of the L-panel splits: the persistent tensor-core launch
+// leaves room on every SM for a split CTA, and the splits (HBM-bound, on L
+// and the inverted blocks only) run beside the launch before the one that
+// needs them.  launched[t & 1] marks launch t done, split[b & 1] block b's
+// operands ready; the side stream starts after everything already on st.
+int tc_side_open(TcSide &side, cudaStream_t st) {
+    cudaError_t e = cudaStreamCreateWithFlags(&side.s, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&side.launched[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.split[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(side.start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.start, 0);
+    return cuda_status(e);
+}
+
+void tc_side_close(TcSide &side) {
+    // released once their pending work is done
+    for (int i = 0; i < 2; ++i) {
+        if (side.launched[i]) cudaEventDestroy(side.launched[i]);
+        if (side.split[i]) cudaEventDestroy(side.split[i]);
+    }
+    if (side.start) cudaEventDestroy(side.start);
+    if (side.s) cudaStreamDestroy(side.s);
+    side = TcSide();
+}
+
+// W_0 = L_panel_0 D_0^-1 and the split of R_0, before step 0; block 1's W
+// operands too (launch 0 needs them before the side stream could make them).
+// This launch counts as launch -1 for the side stream (it reads block 0's
+// operand buffers, which block 2's overwrite).
+int tc_fused_prepare_side(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
+                          const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
     int rc = split_rows(B, ldb, n, nb, f.xs_hi[0], f.xs_lo[0], nb, st);  // columns of R_0
+    if (!rc) rc = tc_w_splits(f, 0, m, nb, L, lda, W, st);
+    if (!rc && 2 * nb < m) rc = tc_w_splits(f, 1, m, nb, L, lda, W, st);
     if (rc) return rc;
     TcLaunch P;
-    rc = tc_w_problem(P.p[0], f, 0, m, nb, L, lda, W, st);
-    return rc ? rc : tc_launch(P, 1, st);
+    rc = tc_w_problem(P.p[0], f, 0, m, nb);
+    if (!rc) rc = tc_launch(P, 1, st);
+    if (!rc && side) rc = cuda_status(cudaEventRecord(side->launched[1], st));
+    return rc;
 }
 
 // Step t: one launch of update t (leaving R_{t+1} split), W_{t+1} and apply
 // t-1; the last step: apply t and apply t-1.  alpha enters through block 0.
-int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st) {
+// With `side`, block t+2's W operands are made on the side stream once
+// launch t-1 is done (their buffers were last read by it), and launch t
+// waits for block t+1's.
+int tc_fused_step_side(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
+                       float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, TcSide *side) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
     const int64_t tb = (m + nb - 1) / nb, r0 = t * nb;
     int rc;
+    cudaError_t e = cudaSuccess;
+    if (side && r0 + 3 * nb < m) {  // block t+2 has rows below it
+        // launch t-1 (t = 0: the preparation's) last read these buffers
+        if ((e = cudaStreamWaitEvent(side->s, side->launched[(t + 1) & 1], 0)) != cudaSuccess) return cuda_status(e);
+        if ((rc = tc_w_splits(f, t + 2, m, nb, L, lda, W, side->s))) return rc;
+        if ((e = cudaEventRecord(side->split[(t + 2) & 1], side->s)) != cudaSuccess) return cuda_status(e);
+    }
     TcLaunch P;
     int np = 0;
     if (t + 1 < tb) {
@@ -534,15 +591,32 @@ int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, i
         if ((rc = tc_problem(P.p[np++], f.wp_hi[t & 1], f.wp_lo[t & 1], f.ra, f.xs_hi[t % 3], f.xs_lo[t % 3], f.rx,
                              nb, g)))
             return rc;
-        if (r0 + 2 * nb < m && (rc = tc_w_problem(P.p[np++], f, t + 1, m, nb, L, lda, W, st))) return rc;
-    } else if ((rc = tc_x_problem(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : 1.f, f.d1_hi, f.d1_lo,
-                                  st))) {
+        if (r0 + 2 * nb < m) {  // block t+1 has rows below it: its W product
+            if (!side && (rc = tc_w_splits(f, t + 1, m, nb, L, lda, W, st))) return rc;
+            if (side && t + 1 >= 2 && (e = cudaStreamWaitEvent(st, side->split[(t + 1) & 1], 0)) != cudaSuccess)
+                return cuda_status(e);
+            if ((rc = tc_w_problem(P.p[np++], f, t + 1, m, nb))) return rc;
+        }
+    } else if ((rc = tc_x_problem(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : 1.f, f.d1_hi[0],
+                                  f.d1_lo[0], st))) {
         return rc;
     }
     if (t >= 1 &&
         (rc = tc_x_problem(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : 1.f, f.d0_hi, f.d0_lo, st)))
         return rc;
-    return tc_launch(P, np, st);
+    if ((rc = tc_launch(P, np, st))) return rc;
+    if (side && (e = cudaEventRecord(side->launched[t & 1], st)) != cudaSuccess) return cuda_status(e);
+    return TRSM_SUCCESS;
+}
+
+int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
+                     int64_t ldb, void *panels, cudaStream_t st) {
+    return tc_fused_prepare_side(m, n, nb, L, lda, W, B, ldb, panels, st, nullptr);
+}
+
+int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
+                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st) {
+    return tc_fused_step_side(t, m, n, nb, L, lda, W, B, ldb, alpha, panels, st, nullptr);
 }
 
 // ---------------------------------------------------------------------------
