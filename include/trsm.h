@@ -212,9 +212,7 @@ int trsm_general(trsm_dtype_t dtype, trsm_side_t side, trsm_uplo_t uplo, trsm_op
  * costs the m^3 flops of that solve rather than TRTRI's m^3/3; the
  * diagonal-block inverses of "Hierarchical Shared Memory-Aware Optimization
  * for TRSM on GPU Platforms" are its first phase.  Ainv must not overlap A.
- * A zero on the diagonal gives IEEE infinities / NaN, no status.  m is
- * limited to 65535 (one grid row per column of the identity); larger m
- * returns -2.
+ * A zero on the diagonal gives IEEE infinities / NaN, no status.
  *
  * Arguments: 1 dtype, 2 m, 3 A, 4 lda, 5 Ainv, 6 ldinv, 7 stream.
  */
