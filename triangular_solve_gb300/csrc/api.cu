@@ -130,7 +130,7 @@ int solve(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const 
         return rc;
     }
 
-    if (m == 128 && layout == TRSM_COL_MAJOR && n > 8) {
+    if (m == 128 && layout == TRSM_COL_MAJOR && n > 8 && n <= 64LL * 65535) {  // column grid: 65535 rows
         // a medium system fits on chip: the whole batch in one launch of the
         // small regime's chunked kernel instead of the blocked path system by
         // system (falls through when its alignment preconditions fail)
