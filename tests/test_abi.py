@@ -85,6 +85,45 @@ def test_workspace_bytes_lookahead_form(lib):
         r(3 * nb * nb * 4) + 2 * r(nb * 300 * 4) + 2 * r(520 * nb * 4) + 4 * r(300 * nb * 4)
 
 
+def test_lookahead_gates_at_their_boundaries(lib):
+    """The look-ahead forms' gates, seen through the workspace they need:
+    f32 from n = 256 columns; c64 from n = 256 up to n = 8192 (above that the
+    per-block flow stays, measured faster once the split block row exceeds
+    twice the L2)."""
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    m, nb = 1000, 256
+    rows = 1024  # m rounded up to 256
+
+    def base(n, eb):
+        return r(4 * nb * nb * eb) + 2 * r(nb * ((n + 3) // 4 * 4) * eb)
+
+    def f32_per_block(n):
+        return 2 * r(m * nb * 4) + 4 * r(n * nb * 4)
+
+    def f32_fused(n):
+        return 8 * r(rows * nb * 4) + 6 * r(r(n) * nb * 4) + 6 * r(nb * nb * 4)
+
+    assert tg.trsm_llnn_workspace_bytes("f32", m, 255, nb) == base(255, 4) + f32_per_block(255)
+    assert tg.trsm_llnn_workspace_bytes("f32", m, 256, nb) == base(256, 4) + max(f32_per_block(256), f32_fused(256))
+
+    def c64_per_block(mm, n, b):
+        return 2 * r(mm * 2 * b * 4) + 4 * r(2 * n * 2 * b * 4)
+
+    def c64_fused(mm, n, b):
+        ra, rx = r(mm), r(n)
+        return 4 * r(ra * 2 * b * 4) + 2 * r(2 * ra * 2 * b * 4) + 6 * r(2 * rx * 2 * b * 4) + 4 * r(b * 2 * b * 4)
+
+    mm, b = 16384, 512
+    tbk = mm // b
+
+    def base64(n):
+        return r(tbk * b * b * 8) + 2 * r(b * ((n + 3) // 4 * 4) * 8)
+
+    assert tg.trsm_llnn_workspace_bytes("c64", mm, 8192, b) == \
+        base64(8192) + max(c64_per_block(mm, 8192, b), c64_fused(mm, 8192, b))
+    assert tg.trsm_llnn_workspace_bytes("c64", mm, 8193, b) == base64(8193) + c64_per_block(mm, 8193, b)
+
+
 def test_status_strings(lib):
     assert tg.trsm_status_string(0) == "success"
     assert "invalid argument" in tg.trsm_status_string(-3)
