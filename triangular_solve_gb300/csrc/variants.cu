@@ -1,8 +1,9 @@
 // Every TRSM variant (left or right side, lower or upper triangle, A, A^T or
 // A^H, unit or non-unit diagonal) through the tuned left / lower /
-// non-transposed / non-unit solve.  The pages name these "other TRSM
-// variants" and leave them open; each is the same solve after a change of
-// variables:
+// non-transposed / non-unit solve.  The summary of "Hierarchical Shared
+// Memory-Aware Optimization for TRSM on GPU Platforms" lists the other TRSM
+// variants among its open questions; each is the same solve after a change
+// of variables:
 //   right side   X op(A) = alpha B  <=>  op(A)^T X^T = alpha B^T, a left-side
 //                problem on B^T with the matrix op(A)^T;
 //   upper        U Y = C  <=>  (J U J)(J Y) = J C with J the order reversal,
