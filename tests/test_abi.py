@@ -237,6 +237,21 @@ def test_general_variant_argument_errors_and_quick_returns(lib):
     assert f(1, 1, 1, 2, 1, 4, 0, one, None, 1, None, 4, None) == 0
 
 
+def test_general_variant_flags_in_the_binding():
+    """side / uplo / trans / diag accept the BLAS letters (either case) or the
+    header's enum values, and refuse anything else before the library is
+    called."""
+    assert tg._flag(tg._SIDE, "r", "side") == 1 and tg._flag(tg._SIDE, 0, "side") == 0
+    assert tg._flag(tg._UPLO, "U", "uplo") == 1
+    assert tg._flag(tg._OP, "c", "trans") == 2 and tg._flag(tg._OP, "T", "trans") == 1
+    assert tg._flag(tg._DIAG, "u", "diag") == 1
+    for table, bad in ((tg._SIDE, "X"), (tg._UPLO, 2), (tg._OP, "H"), (tg._DIAG, None)):
+        with pytest.raises(ValueError):
+            tg._flag(table, bad, "flag")
+    with pytest.raises(ValueError):
+        tg.trsm_general("f32", "Q", "L", "N", "N", 4, 4, 1.0, None, 4, None, 4)
+
+
 def test_small_regime_rejects_too_many_columns(lib):
     one = ctypes.byref(ctypes.c_double(1.0))
     fake = 1 << 20
