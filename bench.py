@@ -9,15 +9,19 @@ small-regime kernel).  Metric: GFLOPS counted as m^2 n real flops per system
 (x4 for complex), summed over the step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--large] [--nb-sweep] [--no-cpu-baseline]
+                    [--no-configs] [--nb-sweep] [--no-cpu-baseline]
 
 With N > 1 (torchrun, one rank per GPU) every rank solves its own batches
 (independent systems, no collective on the data path): weak scaling.
 
 --impl reference times the CPU oracle (plain forward substitution, f64
 accumulation, all host cores) on a bounded sample of the same workload.
---large adds the blocked-path workloads (m = n = 16384 f32 / complex64 with
-the table's NB) to the JSON line under "detail".
+By default the line also carries, under "configs", the rest of the metric:
+the small-regime sweep at batch 16384 (m = n in {8..64} x four types, f32
+m = 64 with n in {1, 6, 10, 32}; GB/s) and the large blocked solves (f32 /
+complex64 m = n = 16384, f64 / complex128 m = n = 8192; GFLOPS against the
+pipe their products run on), each with its roofline fraction and the oracle
+timed on a sample (--no-configs skips them).
 --nb-sweep times the blocked path for NB in {128, 256, 512} over m in
 {1024, 2048, 4096, 8192, 16384} and the four types, and prints the table.
 """
@@ -51,8 +55,10 @@ SQUARE_KERNEL = {"f32": "small_tma_f32_kernel<64, 2>", "f64": "small_fast_kernel
 SQUARE_TRAFFIC_KEY = {"f32": "small_tma_f32_kernel", "f64": "small_fast_kernel<f64>",
                       "c64": "small_fast_kernel<c64>", "c128": "small_fast_kernel<c128>"}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
-FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike)
-TF32_PEAK_TFLOPS = 1100.0        # nominal dense TF32 tensor rate; 3xTF32 costs three products
+FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike); no measured figure
+# nominal dense tensor rates of one GB300 (TFLOP/s): their ratio scales the
+# measured bf16 GEMM rate to the TF32 rate the f32 / c64 products run at
+NOMINAL_BF16_TFLOPS, NOMINAL_TF32_TFLOPS = 2250.0, 1100.0
 SM_COUNT, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
 
 
@@ -60,6 +66,18 @@ def fp32_alu_peak_tflops():
     """FFMA peak from unit counts and the maximum SM clock: 152 SMs x 128
     FP32 lanes x 2 flops x 2.07 GHz."""
     return SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+
+
+def tf32_peaks(peaks, src):
+    """TF32 tensor rate: measured bf16 GEMM rate x the nominal TF32 / bf16
+    ratio (1100 / 2250), burst and sustained; a 3xTF32 (f32-accurate)
+    product costs three TF32 products, so its ceiling is a third of that."""
+    ratio = NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS
+    burst = peaks["bf16_tflops"] * ratio
+    sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
+    how = (f"bf16_tflops ({src}) x {NOMINAL_TF32_TFLOPS:.0f}/{NOMINAL_BF16_TFLOPS:.0f} (nominal TF32/bf16) "
+           f"/ 3 (3xTF32 = three TF32 products)")
+    return burst, sustained, how
 
 
 def measured_peaks():
@@ -399,8 +417,13 @@ def run_gb300(args, ws, rank, local):
         "wall_s_timed_region": round(wall, 4),
         "detail": detail,
     }
-    if args.large and rank == 0:
-        out["detail"]["large"] = run_large(torch, tg, dev, stream, peaks)
+    if rank == 0 and not args.no_configs:
+        # the rest of the metric: the batch-16384 small sweep (GB/s) and the
+        # large blocked solves, each with its roofline and oracle baseline
+        out["configs"] = {
+            "small_sweep_b16384": config_small_sweep(torch, tg, dev, stream, flush, peaks, peak_src),
+            "large_blocked": config_large(torch, tg, dev, stream, peaks, peak_src),
+        }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     if dist is not None:
@@ -410,51 +433,159 @@ def run_gb300(args, ws, rank, local):
         print(json.dumps(out), flush=True)
 
 
-def run_large(torch, tg, dev, stream, peaks, reps=2):
-    """Blocked-path workloads with the table's NB: m = n = 16384 in f32 and
-    complex64 (alpha = 1), m = n = 8192 in f64 and complex128 (alpha = 1.5)."""
+def _events(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def fp32_roof(d):
+    """Arithmetic ceiling (TFLOP/s) of a small-regime type and its source."""
+    if d in ("f64", "c128"):
+        return FP64_PEAK_TFLOPS, "nominal GB300 FP64 rate (recipe table)"
+    return fp32_alu_peak_tflops(), "FP32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz (unit counts, max clock)"
+
+
+def config_small_sweep(torch, tg, dev, stream, flush, peaks, peak_src, reps=5, sample=1024):
+    """The small-regime sweep: m = n in {8, 16, 32, 48, 64} x four types and
+    f32 m = 64 with n in {1, 6, 10, 32}, strided batch 16384 (column-major,
+    lda = ldb = m, L strictly lower U(-1,1)/64, diagonal 1 + U(0,1), B
+    U(-1,1), alpha = 1).  Per point: CUDA-event time of one launch (L2
+    flushed and B restored before each), GB/s of the algorithmic bytes,
+    GFLOPS, the roofline time max(bytes / HBM, flops / pipe) over the measured
+    time, and the oracle on a sample of the same batch."""
+    import oracle
+    batch = 16384
+    points = [(d, mm, mm) for d in DTYPES for mm in (8, 16, 32, 48, 64)]
+    points += [("f32", 64, nn) for nn in (1, 6, 10, 32) if "f32" in DTYPES]
     res = {}
-    for d, mm, alpha in (("f32", 16384, 1.0), ("c64", 16384, 1.0), ("f64", 8192, 1.5), ("c128", 8192, 1.5)):
-        L, B = ti.generate(d, mm, mm, 1, kind="ddm")
+    for d, mm, nn in points:
+        L, B = ti.generate(d, mm, nn, batch, kind="dd64")
         a = torch.from_numpy(ti.to_storage(L, "col")).to(dev)
         b0 = torch.from_numpy(ti.to_storage(B, "col")).to(dev)
-        del L, B
+        b = torch.empty_like(b0)
+
+        def launch():
+            tg.trsm_llnn_strided_batched(d, "col", mm, nn, 1.0, a, mm, mm * mm, b, mm, mm * nn, batch, stream)
+
+        for _ in range(2):
+            b.copy_(b0)
+            launch()
+        times = []
+        for _ in range(reps):
+            b.copy_(b0)
+            flush.fill_(len(times) + 1)
+            e0, e1 = _events(torch)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.mean(times)
+        q, f = ti.algorithmic_bytes(d, mm, nn, batch), ti.flops(d, mm, nn, batch)
+        p_tf, p_src = fp32_roof(d)
+        t_hbm = q / (peaks["hbm_gbs"] * 1e9) * 1e3
+        t_alu = f / (p_tf * 1e12) * 1e3
+        if t_hbm >= t_alu:
+            roof = {"bound": "hbm", "achieved": round(q / (ms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "peak_source": f"hbm_gbs ({peak_src})"}
+        else:
+            roof = {"bound": "alu", "achieved": round(f / (ms * 1e-3) / 1e12, 3), "peak": round(p_tf, 2),
+                    "unit": "TFLOP/s", "peak_source": p_src}
+        roof["frac"] = round(max(t_hbm, t_alu) / ms, 4)
+        # the oracle on the first `sample` systems of the batch
+        a_h = ti.to_storage(L[:sample], "col")
+        b_h = ti.to_storage(B[:sample], "col")
+        t0 = time.perf_counter()
+        oracle.trsm_llnn(d, mm, nn, 1.0, a_h, mm, b_h, mm, stride_a=mm * mm, stride_b=mm * nn, batch=sample)
+        el = time.perf_counter() - t0
+        res[f"{d}_m{mm}_n{nn}"] = {
+            "dtype": d, "m": mm, "n": nn, "batch": batch, "ms": round(ms, 5),
+            "gbs": round(q / (ms * 1e-3) / 1e9, 1), "gflops": round(f / (ms * 1e-3) / 1e9, 1),
+            "roofline": roof,
+            "cpu_baseline": {"value": round(ti.flops(d, mm, nn, sample) / el / 1e9, 3), "unit": "GFLOPS",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{sample} of the {batch} systems, {el * 1e3:.1f} ms"},
+        }
+        del a, b0, b, L, B
+    torch.cuda.empty_cache()
+    return res
+
+
+def config_large(torch, tg, dev, stream, peaks, peak_src, which=None, reps=2):
+    """The blocked path on the large workloads, table NB: f32 and complex64
+    at m = n = 16384 (alpha = 1), f64 and complex128 at m = n = 8192
+    (alpha = 1.5); L strictly lower U(-1,1)/m, diagonal 1 + U(0,1), B U(-1,1),
+    column-major.  Per workload: CUDA-event time of one solve (after a
+    warm-up solve), GFLOPS (m^3, x4 complex), the fraction of the pipe the
+    products run on, the inversion / apply / update split, and the oracle on
+    64 sampled right-hand-side columns -- timed (the CPU baseline) and
+    compared with the GPU's X on those columns."""
+    import oracle
+    tf_burst, tf_sus, tf_how = tf32_peaks(peaks, peak_src)
+    res = {}
+    work = [("f32", 16384, 1.0), ("c64", 16384, 1.0), ("f64", 8192, 1.5), ("c128", 8192, 1.5)]
+    for d, mm, alpha in work:
+        if d not in DTYPES or (which and d not in which):
+            continue
+        L, B = ti.generate(d, mm, mm, 1, kind="ddm")
+        # the logical (row-major) arrays are the column-major storage of the
+        # transposes; transposing on the device gives column-major L and B
+        a = torch.from_numpy(L[0]).to(dev).t().contiguous().t()
+        b0 = torch.from_numpy(B[0]).to(dev).t().contiguous().t()
+        cols = ti.sample_columns(mm)
         b = torch.empty_like(b0)
         nb = tg.trsm_llnn_select_nb(d, mm, mm)
         wsb = tg.trsm_llnn_workspace_bytes(d, mm, mm, nb)
         wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
         b.copy_(b0)
         tg.trsm_llnn_ex(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)  # warm-up
-        times, phases = [], []
+        times = []
         for _ in range(reps):
             b.copy_(b0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0, e1 = _events(torch)
             e0.record(stream)
             tg.trsm_llnn_ex(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)
             e1.record(stream)
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
+        x_cols = b[:, torch.from_numpy(cols).to(dev)].cpu().numpy()
         b.copy_(b0)
         phases = tg.trsm_llnn_profile(d, mm, mm, alpha, a, mm, b, mm, nb, wsp, wsb, stream)
-        ms = statistics.mean(times)
-        gf = ti.flops(d, mm, mm) / (ms * 1e-3) / 1e9
-        tot = sum(phases)
-        fp64 = d in ("f64", "c128")
-        # f32 / c64: the GEMMs run on the tensor cores as 3xTF32 products, whose
-        # f32-accurate ceiling is a third of the TF32 rate
-        peak = FP64_PEAK_TFLOPS if fp64 else TF32_PEAK_TFLOPS / 3
-        res[f"{d}_m{mm}"] = {
-            "nb": nb, "ms": round(ms, 3), "gflops": round(gf, 1),
-            "pipe": "FP64 (DFMA)" if fp64 else "tensor (tcgen05 kind::tf32, 3xTF32)",
-            "peak_tflops": round(peak, 1),
-            "frac_of_pipe_peak": round(gf / 1e3 / peak, 4),
-            **({} if fp64 else {"frac_of_fp32_fma_peak": round(gf / 1e3 / fp32_alu_peak_tflops(), 4)}),
-            "phase_share": {"diag_inversion": round(phases[0] / tot, 4),
-                            "block_apply": round(phases[1] / tot, 4),
-                            "gemm_update": round(phases[2] / tot, 4)},
-        }
         del a, b0, b, wsp
         torch.cuda.empty_cache()
+        # the oracle on the sampled columns (row-major storage of the same values)
+        bs = np.ascontiguousarray(B[0][:, cols])
+        t0 = time.perf_counter()
+        oracle.trsm_llnn(d, mm, len(cols), alpha, L[0], mm, bs, len(cols), layout="row")
+        el = time.perf_counter() - t0
+        t = np.complex128 if ti.IS_COMPLEX[d] else np.float64
+        err = float(np.linalg.norm((x_cols.astype(t) - bs.astype(t)).ravel()) / np.linalg.norm(bs.astype(t).ravel()))
+        tol = 1e-5 if d in ("f32", "c64") else 1e-12
+        del L, B
+        ms = statistics.mean(times)
+        fl = ti.flops(d, mm, mm)
+        tfs = fl / (ms * 1e-3) / 1e12
+        tot = sum(phases) or 1.0
+        if d in ("f64", "c128"):
+            roof = {"bound": "alu", "achieved": round(tfs, 3), "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s",
+                    "frac": round(tfs / FP64_PEAK_TFLOPS, 4), "pipe": "FP64 (DFMA)",
+                    "peak_source": "nominal GB300 FP64 rate (recipe table); no measured FP64 peak"}
+        else:
+            roof = {"bound": "tensor", "achieved": round(tfs, 2), "peak": round(tf_burst / 3, 1),
+                    "unit": "TFLOP/s", "frac": round(tfs / (tf_burst / 3), 4),
+                    "frac_of_sustained": round(tfs / (tf_sus / 3), 4),
+                    "pipe": "tensor (tcgen05 kind::tf32, 3xTF32 split)", "peak_source": tf_how,
+                    "frac_of_fp32_fma_peak": round(tfs / fp32_alu_peak_tflops(), 3)}
+        res[f"{d}_m{mm}"] = {
+            "dtype": d, "m": mm, "n": mm, "alpha": alpha, "nb": nb, "ms": round(ms, 3),
+            "gflops": round(fl / (ms * 1e-3) / 1e9, 1), "roofline": roof,
+            "phase_share": {"diag_inversion": round(phases[0] / tot, 4), "block_apply": round(phases[1] / tot, 4),
+                            "gemm_update": round(phases[2] / tot, 4)},
+            "parity": {"rel_fro_sampled_cols": err, "tol": tol, "ok": bool(err <= tol),
+                       "columns": "default_rng(1).choice(n, 64, replace=False), sorted"},
+            "cpu_baseline": {"value": round(ti.flops(d, mm, len(cols)) / el / 1e9, 3), "unit": "GFLOPS",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"the 64 sampled right-hand-side columns of this system, {el:.1f} s"},
+        }
     return res
 
 
@@ -511,6 +642,48 @@ def variants_bench(args):
             torch.cuda.empty_cache()
 
 
+def medium_bench(args):
+    """One JSON line per (type, m): a strided batch of --batch systems of
+    order m (n = m, column-major, contiguous, L strictly lower U(-1,1)/m,
+    diagonal 1 + U(0,1), B U(-1,1), alpha = 1) through
+    trsm_llnn_strided_batched; CUDA events on the launching stream after a
+    warm-up call, inputs resident, B restored before every run; GFLOPS credit
+    m^2 n per system (x4 complex)."""
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    batch = args.batch
+    for d in args.sweep_dtypes.split(","):
+        for mm in [int(x) for x in args.sweep_ms.split(",")]:
+            L, B = ti.generate(d, mm, mm, batch, kind="ddm")
+            a = torch.from_numpy(ti.to_storage(L, "col")).to(dev)
+            b0 = torch.from_numpy(ti.to_storage(B, "col")).to(dev)
+            del L, B
+            b = b0.clone()
+            tg.trsm_llnn_strided_batched(d, "col", mm, mm, 1.0, a, mm, mm * mm, b, mm, mm * mm, batch, stream)
+            times = []
+            for _ in range(max(args.sweep_reps, 1)):
+                b.copy_(b0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                tg.trsm_llnn_strided_batched(d, "col", mm, mm, 1.0, a, mm, mm * mm, b, mm, mm * mm, batch, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.mean(times)
+            print(json.dumps({"op": "strided_batched", "dtype": d, "m": mm, "n": mm, "batch": batch,
+                              "ms": round(ms, 4),
+                              "gflops": round(ti.flops(d, mm, mm, batch) / (ms * 1e-3) / 1e9, 1),
+                              "gbs": round(ti.algorithmic_bytes(d, mm, mm, batch) / (ms * 1e-3) / 1e9, 1)}),
+                  flush=True)
+            del a, b0, b
+            torch.cuda.empty_cache()
+
+
 def trtri_bench(args):
     """One JSON line per (type, m): the triangular inverse L^-1 through
     trsm_trtri_lower (set to I, then the L X = I solve), CUDA events on the
@@ -545,23 +718,6 @@ def trtri_bench(args):
                               "gflops_solve": round(cplx * mm ** 3 / (ms * 1e-3) / 1e9, 1)}), flush=True)
             del a, x
             torch.cuda.empty_cache()
-
-
-def pipe_peaks():
-    """TFLOP/s of dependent-free FMA loops on every SM: FP32 FMA, paired FP32
-    FMA, FP64 FMA and the FP64 warp MMA (m8n8k4), three measurements each."""
-    import ctypes
-
-    from triangular_solve_gb300 import build as tgb
-    tgb.build()
-    lib = ctypes.CDLL(tgb.PROBE_LIB)
-    lib.trsm_probe_pipe_tflops.argtypes = [ctypes.c_int, ctypes.c_int]
-    lib.trsm_probe_pipe_tflops.restype = ctypes.c_double
-    out = {}
-    for kind, name in ((0, "ffma"), (3, "ffma2"), (1, "dfma"), (2, "dmma")):
-        out[name] = [round(lib.trsm_probe_pipe_tflops(kind, 10), 3) for _ in range(3)]
-    print(json.dumps({"pipe_tflops": out}), flush=True)
-    return out
 
 
 def nb_sweep(args):
@@ -711,12 +867,11 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
-    ap.add_argument("--large", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the small sweep (batch 16384) and the large blocked solves")
     ap.add_argument("--nb-sweep", action="store_true")
     ap.add_argument("--sweep-dtypes", default="f32,f64,c64,c128")
     ap.add_argument("--sweep-ms", default="1024,2048,4096,8192,16384")
-    ap.add_argument("--pipe-peaks", action="store_true",
-                    help="measure the FFMA / paired-FFMA / DFMA / DMMA pipe rates (csrc/probe/pipe_peaks.cu)")
     ap.add_argument("--sweep-reps", type=int, default=3)
     ap.add_argument("--sweep-nbs", default="128,256,512", help="block sizes of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -725,6 +880,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--variants", action="store_true",
                     help="time every TRSM variant (trsm_general) at m = n = --sweep-ms per --sweep-dtypes")
+    ap.add_argument("--medium", action="store_true",
+                    help="time strided batches (--batch) of m = n = --sweep-ms systems per --sweep-dtypes")
+    ap.add_argument("--batch", type=int, default=1024)
     ap.add_argument("--trtri", action="store_true",
                     help="time the exported triangular inverse (trsm_trtri_lower) at --sweep-ms per --sweep-dtypes")
     args = ap.parse_args()
@@ -738,11 +896,11 @@ def main():
     if args.nb_sweep:
         nb_sweep(args)
         return
-    if args.pipe_peaks:
-        pipe_peaks()
-        return
     if args.trtri:
         trtri_bench(args)
+        return
+    if args.medium:
+        medium_bench(args)
         return
     if args.variants:
         variants_bench(args)

@@ -110,10 +110,17 @@ int trsm_llnn_strided_batched(trsm_dtype_t dtype, trsm_layout_t layout, int64_t 
  * The pages describe no such entry point; it exists for callers whose data
  * lives in host memory.
  *
- * The batch is cut into up to eight chunks that alternate between two
- * internal streams: while one chunk is being solved, the next one is copied
- * in and the previous one copied out.  Device buffers for two chunks come
- * from cudaMallocAsync on `stream` and are released on it.  The call is
+ * The batch is cut into up to eight chunks that flow through a three-stage
+ * pipeline -- host-to-device copy, solve, device-to-host copy -- on three
+ * internal streams, so the copy in of one chunk, the solve of the previous
+ * one and the copy out of the one before run at the same time.  The internal
+ * streams are forked from `stream` and joined back to it with events.  They
+ * and a ring of three device buffer sets are kept per (device, caller
+ * stream) for the life of the process: the first call on a stream creates
+ * the streams and allocates the buffers with cudaMalloc; the buffers only
+ * grow, so later calls of the same or smaller size allocate nothing.  A call
+ * that needs larger buffers frees the old ones with cudaFree first, which
+ * waits for the whole device (a synchronising grow).  The call is
  * stream-ordered like the others: it returns once the work is enqueued, and
  * X is in B only when `stream` has reached the end of this call's work
  * (synchronise it before reading B).  A and B must stay valid and B must not
@@ -262,6 +269,19 @@ int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
  * No counterpart on the pages.
  */
 int trsm_device_status(int clear);
+
+/*
+ * Testing hook for the bounded waits: sets how many times the batched f32
+ * small-regime kernel (the one that streams systems through the TMA engine)
+ * polls for each item's copies before it gives up, records
+ * TRSM_ERR_DEVICE_TIMEOUT (see trsm_device_status), lets the copies already
+ * in flight land (those waits keep the full limit), and returns with the
+ * item unsolved.  polls = 0 makes every such wait expire at once, so a test
+ * can exercise the timeout path without a fault or a hang; a negative value
+ * restores the compiled limit.  Applies to launches made after the call, on
+ * every device.  Not for production use.  No counterpart on the pages.
+ */
+int trsm_set_wait_limit(int64_t polls);
 
 /* Static, human-readable text for a status code returned by this library. */
 const char *trsm_status_string(int status);

@@ -195,9 +195,9 @@ def test_lookahead_flow_edges(env, dtype, m, n, nb, ld_pad):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "c64"])
-def test_batched_blocked_tensor_core_systems(env, dtype):
-    """Strided batch of m > 64 systems large enough for the tensor-core apply
-    and update, with padding between systems."""
+def test_batched_blocked_padded_systems(env, dtype):
+    """Strided batch of two m = 640 systems (the batched blocked path), with
+    padding between systems."""
     m, n, batch = 640, 300, 2
     L, B = ti.generate(dtype, m, n, batch, kind="ddm", seed=7)
     a, b, geo = storage_pair(L, B, lda=m + 4, ldb=m + 8, stride_a=m * (m + 4) + 16, stride_b=n * (m + 8) + 32)
@@ -206,4 +206,4 @@ def test_batched_blocked_tensor_core_systems(env, dtype):
     ref = oracle_buffers(dtype, a, b, geo, alpha, env["oracle"])
     assert env["tg"].trsm_device_status() == 0
     assert_padding_untouched(raw, b, geo)
-    assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"batched tc {dtype}")
+    assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"batched padded {dtype}")

@@ -1,5 +1,6 @@
 """trsm_llnn_strided_batched_host -- the strided-batched solve on host
-buffers, pipelined in chunks over two internal streams -- against the oracle,
+buffers, pipelined in chunks over three internal streams (copy in, solve,
+copy out) -- against the oracle,
 through the C ABI: chunked batches, row-major systems with gaps between them,
 one A shared by all systems, the blocked path, alpha = 0."""
 import numpy as np

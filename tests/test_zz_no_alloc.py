@@ -1,9 +1,16 @@
 """trsm_llnn_noalloc -- the entry point for callers that cannot allocate
 device memory (a library inside a host application that owns all device
 memory through its own pool, or a latency-sensitive path on which
-cudaMalloc / cudaFree must not run) -- gives the same X as the allocating
-entry point trsm_llnn, within the parity tolerances, on consecutive calls
-that share its fixed device workspace.
+cudaMalloc / cudaFree must not run) -- on consecutive calls that share its
+fixed device array:
+
+  * its X matches the allocating entry point trsm_llnn and the oracle, within
+    the parity tolerances, on every call of a sequence whose sizes change, so
+    each call starts from the previous call's leftovers in the array;
+  * the sequence reaches the tensor-core look-ahead paths of f32 and c64,
+    whose operand panels and tensor maps then live in the array;
+  * once the array is loaded (first call), a call changes neither the
+    device's free memory nor torch's caching allocator.
 
 Called through the C ABI with ctypes.  Kept in a file of its own that pytest
 collects last; it builds and loads the library itself, so it also passes
@@ -21,10 +28,11 @@ pytestmark = pytest.mark.gpu
 
 SCRATCH_BYTES = 32 * 1024 * 1024  # TRSM_NOALLOC_SCRATCH_BYTES
 ERR_WORKSPACE = 900
+CODE = {"f32": 0, "f64": 1, "c64": 2, "c128": 3}
 
 
 @pytest.fixture(scope="module")
-def env():
+def env(oracle_mod):
     import torch
 
     import triangular_solve_gb300 as tg
@@ -39,10 +47,9 @@ def env():
         fn.restype = ctypes.c_int
     lib.trsm_llnn_workspace_bytes.argtypes = [ctypes.c_int, i64, i64, i64]
     lib.trsm_llnn_workspace_bytes.restype = ctypes.c_size_t
-    return dict(torch=torch, lib=lib)
-
-
-CODE = {"f32": 0, "f64": 1, "c64": 2, "c128": 3}
+    lib.trsm_device_status.argtypes = [ctypes.c_int]
+    lib.trsm_device_status.restype = ctypes.c_int
+    return dict(torch=torch, lib=lib, oracle=oracle_mod)
 
 
 def _alpha(dtype, a):
@@ -55,46 +62,100 @@ def _alpha(dtype, a):
     return ctypes.byref((ctypes.c_double * 2)(a.real, a.imag))
 
 
-def _run(env, fn_name, dtype, L, B, alpha, lda, ldb):
-    """One solve through the named C entry point on fresh device copies."""
-    torch = env["torch"]
-    m, n = B.shape
-    a = ti.to_storage(L[None], "col", lda)
-    b = ti.to_storage(B[None], "col", ldb)
-    tA = torch.from_numpy(a).cuda()
-    tB = torch.from_numpy(b).cuda()
-    stream = torch.cuda.current_stream().cuda_stream
-    rc = getattr(env["lib"], fn_name)(CODE[dtype], m, n, _alpha(dtype, complex(alpha)), tA.data_ptr(),
-                                      lda, tB.data_ptr(), ldb, stream)
-    assert rc == 0, f"{fn_name} returned {rc}"
-    torch.cuda.synchronize()
-    return ti.from_storage(tB.cpu().numpy(), 1, m, n, "col", ldb)[0]
+class Problem:
+    """One system in column-major storage with padded leading dimensions (NaN
+    in A's strictly upper part), resident on the device."""
+
+    def __init__(self, env, dtype, m, n, alpha, seed):
+        torch = env["torch"]
+        L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=seed)
+        self.env, self.dtype, self.m, self.n, self.alpha = env, dtype, m, n, alpha
+        self.lda, self.ldb = m + 1, m + 3
+        Lw = L.copy()
+        Lw[:, np.triu(np.ones((m, m), dtype=bool), 1)] = np.nan
+        self.a = ti.to_storage(Lw, "col", self.lda)
+        self.b = ti.to_storage(B, "col", self.ldb)
+        self.tA = torch.from_numpy(self.a).cuda()
+        self.tB0 = torch.from_numpy(self.b).cuda()
+        self.tB = self.tB0.clone()
+
+    def call(self, fn_name):
+        """Restore B, solve through the named C entry point, return X."""
+        torch = self.env["torch"]
+        self.tB.copy_(self.tB0)
+        torch.cuda.synchronize()
+        rc = getattr(self.env["lib"], fn_name)(
+            CODE[self.dtype], self.m, self.n, _alpha(self.dtype, complex(self.alpha)), self.tA.data_ptr(),
+            self.lda, self.tB.data_ptr(), self.ldb, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, f"{fn_name} returned {rc}"
+        torch.cuda.synchronize()
+        return ti.from_storage(self.tB.cpu().numpy(), 1, self.m, self.n, "col", self.ldb)[0]
+
+    def oracle(self):
+        out = self.b.copy()
+        self.env["oracle"].trsm_llnn(self.dtype, self.m, self.n, self.alpha, self.a, self.lda, out, self.ldb)
+        return ti.from_storage(out, 1, self.m, self.n, "col", self.ldb)[0]
 
 
-# Two consecutive calls per type, the second of a different size, so the
-# second call starts from the first call's leftovers in the shared array.
-CASES = [(700, 50, 1.5), (333, 90, -0.75)]
+def _err(x, ref):
+    return float(per_system_rel_fro(x[None], ref[None])[0])
+
+
+# Consecutive calls per type, sizes changing between calls, so every call
+# starts from the previous call's leftovers in the shared array.  The f32
+# and c64 sequences include a system that takes the tensor-core look-ahead
+# form (n >= 256, several block rows), whose operand panels live in the array.
+SEQUENCES = {
+    "f32": [(700, 50, 1.5), (1024, 1024, 1.0), (333, 90, -0.75)],
+    "f64": [(700, 50, 1.5), (333, 90, -0.75)],
+    "c64": [(700, 50, 1.5), (768, 512, 0.5), (333, 90, -0.75)],
+    "c128": [(700, 50, 1.5), (333, 90, -0.75)],
+}
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f64", "c64", "c128"])
-def test_noalloc_matches_allocating_entry_on_consecutive_calls(env, dtype):
-    for i, (m, n, alpha) in enumerate(CASES):
-        need = env["lib"].trsm_llnn_workspace_bytes(CODE[dtype], m, n, 0)
+def test_noalloc_matches_allocating_entry_and_oracle_on_consecutive_calls(env, dtype):
+    lib = env["lib"]
+    for i, (m, n, alpha) in enumerate(SEQUENCES[dtype]):
+        need = lib.trsm_llnn_workspace_bytes(CODE[dtype], m, n, 0)
         assert 0 < need <= SCRATCH_BYTES
-        L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=40 + i)
         al = complex(alpha, 0.25) if ti.IS_COMPLEX[dtype] else alpha
-        ref = _run(env, "trsm_llnn", dtype, L[0], B[0], al, m + 1, m + 3)
-        got = _run(env, "trsm_llnn_noalloc", dtype, L[0], B[0], al, m + 1, m + 3)
-        assert np.all(np.isfinite(got))
-        err = float(per_system_rel_fro(got[None], ref[None])[0])
-        assert err <= TOL[dtype], f"call {i + 1}: {dtype} m={m} n={n} rel. error {err:.3e}"
+        p = Problem(env, dtype, m, n, al, seed=40 + i)
+        ref = p.call("trsm_llnn")
+        orc = p.oracle()
+        for rep in range(2):  # the same system twice in a row through the array
+            got = p.call("trsm_llnn_noalloc")
+            assert np.all(np.isfinite(got))
+            e_llnn, e_orc = _err(got, ref), _err(got, orc)
+            assert e_llnn <= TOL[dtype], f"call {i + 1}.{rep}: {dtype} m={m} n={n} vs trsm_llnn {e_llnn:.3e}"
+            assert e_orc <= TOL[dtype], f"call {i + 1}.{rep}: {dtype} m={m} n={n} vs oracle {e_orc:.3e}"
+        assert lib.trsm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dtype,m,n", [("f32", 1024, 1024), ("c64", 768, 512), ("f64", 700, 50)])
+def test_noalloc_leaves_device_memory_unchanged(env, dtype, m, n):
+    torch = env["torch"]
+    p = Problem(env, dtype, m, n, 1.0, seed=7)
+    p.call("trsm_llnn")
+    orc = p.oracle()
+    p.call("trsm_llnn_noalloc")  # the array's module and the side stream exist from here on
+    stats0 = torch.cuda.memory_stats()
+    free0, _ = torch.cuda.mem_get_info()
+    got = p.call("trsm_llnn_noalloc")
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0, f"device free memory changed by {free1 - free0} bytes"
+    for key in ("reserved_bytes.all.current", "allocated_bytes.all.current", "num_alloc_retries"):
+        assert stats1.get(key, 0) == stats0.get(key, 0), key
+    assert _err(got, orc) <= TOL[dtype]
 
 
 def test_noalloc_small_regime_needs_no_workspace(env):
-    L, B = ti.generate("f32", 64, 64, 1, kind="dd64")
-    ref = _run(env, "trsm_llnn", "f32", L[0], B[0], 1.0, 64, 64)
-    got = _run(env, "trsm_llnn_noalloc", "f32", L[0], B[0], 1.0, 64, 64)
-    assert float(per_system_rel_fro(got[None], ref[None])[0]) <= TOL["f32"]
+    p = Problem(env, "f32", 64, 64, 1.0, seed=0)
+    ref = p.call("trsm_llnn")
+    got = p.call("trsm_llnn_noalloc")
+    assert _err(got, ref) <= TOL["f32"]
+    assert _err(got, p.oracle()) <= TOL["f32"]
 
 
 def test_noalloc_rejects_problems_beyond_its_array(env):

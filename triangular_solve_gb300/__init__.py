@@ -19,8 +19,9 @@ import re
 import threading
 
 __all__ = [
-    "trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_select_nb", "trsm_llnn_workspace_bytes",
-    "trsm_llnn_ex", "trsm_llnn_profile", "trsm_status_string", "trsm_llnn_noalloc", "trsm_device_status",
+    "trsm_llnn", "trsm_llnn_strided_batched", "trsm_llnn_strided_batched_host", "trsm_llnn_select_nb",
+    "trsm_llnn_workspace_bytes", "trsm_llnn_ex", "trsm_llnn_profile", "trsm_general", "trsm_trtri_lower",
+    "trsm_status_string", "trsm_llnn_noalloc", "trsm_device_status", "trsm_set_wait_limit",
     "solve", "TrsmError",
     "library_path", "load_library",
 ]
@@ -271,6 +272,16 @@ def trsm_device_status(clear: bool = True) -> int:
     fn.argtypes = [ctypes.c_int]
     fn.restype = ctypes.c_int
     return int(fn(1 if clear else 0))
+
+
+def trsm_set_wait_limit(polls: int) -> None:
+    """Testing hook: polls of the batched f32 small kernel's first wait per
+    item (0: expire at once; negative: the compiled limit).  See
+    include/trsm.h."""
+    fn = load_library().trsm_set_wait_limit
+    fn.argtypes = [ctypes.c_int64]
+    fn.restype = ctypes.c_int
+    _check("trsm_set_wait_limit", fn(int(polls)))
 
 
 def trsm_status_string(status: int) -> str:

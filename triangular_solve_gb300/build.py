@@ -19,8 +19,6 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtrsm_gb300.so")
-PROBE_SRC = os.path.join(CSRC, "probe", "pipe_peaks.cu")
-PROBE_LIB = os.path.join(BUILD, "libtrsm_peaks.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -77,13 +75,6 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp, LIB)
-    if force or not os.path.exists(PROBE_LIB) or os.path.getmtime(PROBE_LIB) < os.path.getmtime(PROBE_SRC):
-        tmp = PROBE_LIB + f".tmp{os.getpid()}"
-        r = subprocess.run([nvcc(), *ARCH, *FLAGS, "-shared", "-o", tmp, PROBE_SRC],
-                           capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"probe build failed:\n{r.stderr}")
-        os.replace(tmp, PROBE_LIB)
     if verbose_ptxas:
         print("\n".join(logs))
     return LIB

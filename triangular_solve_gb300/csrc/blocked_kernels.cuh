@@ -65,7 +65,10 @@ struct InvL1Steps {
 
 template <typename T, int IB>
 __global__ void __launch_bounds__(IB) inv_diag_l1_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
-                                                         T *__restrict__ W) {
+                                                         T *__restrict__ W, int64_t sL = 0, int64_t sW = 0) {
+    // grid y: systems of a batch (L and W advance by sL / sW elements)
+    L += (int64_t)blockIdx.y * sL;
+    W += (int64_t)blockIdx.y * sW;
     __shared__ __align__(16) T buf[2][IB];
     const int t = blockIdx.x / 8, i = blockIdx.x % 8;
     const int tid = threadIdx.x;
@@ -191,7 +194,10 @@ __device__ __forceinline__ void inv_offdiag_block(const T *__restrict__ L, int64
 
 template <typename T, int IB>
 __global__ void __launch_bounds__(256) inv_offdiag_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int nb,
-                                                          T *__restrict__ W) {
+                                                          T *__restrict__ W, int64_t sL = 0, int64_t sW = 0) {
+    // grid z: systems of a batch
+    L += (int64_t)blockIdx.z * sL;
+    W += (int64_t)blockIdx.z * sW;
     for (int d = 1; d < 8 - (int)blockIdx.y; ++d) {
         inv_offdiag_block<T, IB>(L, lda, m, nb, W, d);
         __syncthreads();  // Y_ij is read by the next sub-block of this column
@@ -233,6 +239,7 @@ struct GemmArgs {
     int beta_zero, a_lower;
     int b_rowmajor;  // B element (k, c) at k*ldb + c instead of c*ldb + k
     int c_rowmajor;  // C element (r, c) at r*ldc + c instead of c*ldc + r
+    int64_t sA = 0, sB = 0, sC = 0;  // grid z: systems of a batch, element strides
 };
 
 template <typename T, bool SMALL>
@@ -248,6 +255,9 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
     const int tid = threadIdx.x;
     const int tx = tid % (BM / TM), ty = tid / (BM / TM);
     const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN;
+    const T *gA = g.A + (int64_t)blockIdx.z * g.sA;
+    const T *gB = g.B + (int64_t)blockIdx.z * g.sB;
+    T *gC = g.C + (int64_t)blockIdx.z * g.sC;
     int64_t kend = g.K;
     if (g.a_lower && m0 + BM < kend) kend = m0 + BM;
     const int nk = (int)((kend + BK - 1) / BK);
@@ -257,21 +267,21 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
         for (int e = tid; e < BM * BK; e += NT) {
             const int kk = e / BM, r = e % BM;
             const int64_t gr = m0 + r, gk = k0 + kk;
-            if (gr < g.M && gk < kend) cp_async<sizeof(T)>(&As[s][kk][r], g.A + gk * g.lda + gr);
+            if (gr < g.M && gk < kend) cp_async<sizeof(T)>(&As[s][kk][r], gA + gk * g.lda + gr);
             else As[s][kk][r] = zero_of<T>();
         }
         if (g.b_rowmajor) {
             for (int e = tid; e < BK * BN; e += NT) {
                 const int kk = e / BN, c = e % BN;
                 const int64_t gc = n0 + c, gk = k0 + kk;
-                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gk * g.ldb + gc);
+                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], gB + gk * g.ldb + gc);
                 else Bs[s][kk][c] = zero_of<T>();
             }
         } else {
             for (int e = tid; e < BK * BN; e += NT) {
                 const int kk = e % BK, c = e / BK;
                 const int64_t gc = n0 + c, gk = k0 + kk;
-                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], g.B + gc * g.ldb + gk);
+                if (gc < g.N && gk < kend) cp_async<sizeof(T)>(&Bs[s][kk][c], gB + gc * g.ldb + gk);
                 else Bs[s][kk][c] = zero_of<T>();
             }
         }
@@ -315,7 +325,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
         for (int x = 0; x < TM; ++x) {
             const int64_t gr = m0 + tx * TM + x;
             if (gr >= g.M) continue;
-            T *cp = g.c_rowmajor ? g.C + gr * g.ldc + gc : g.C + gc * g.ldc + gr;
+            T *cp = g.c_rowmajor ? gC + gr * g.ldc + gc : gC + gc * g.ldc + gr;
             T v = mul(g.gamma, acc[x][y]);
             if (!g.beta_zero) v = fma_(g.beta, *cp, v);
             *cp = v;
@@ -328,7 +338,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GemmArgs<T> g) {
 // src[r*ld_src + c].  32 x 32 tiles through shared memory.
 template <typename T>
 __global__ void transpose_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst, int64_t ld_dst,
-                                 int64_t rows, int64_t cols) {
+                                 int64_t rows, int64_t cols, int64_t s_src = 0, int64_t s_dst = 0) {
+    // grid z: systems of a batch
+    src += (int64_t)blockIdx.z * s_src;
+    dst += (int64_t)blockIdx.z * s_dst;
     __shared__ T tile[32][33];
     const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
     for (int q = threadIdx.y; q < 32; q += blockDim.y) {

@@ -13,10 +13,10 @@ namespace trsm {
 // Generic GEMM: the regular tiles when they fill two waves of SMs, else
 // the small tiles.
 template <typename T>
-static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
+static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st, int nz = 1) {
     using C = GemmCfg<T, false>;
     using S = GemmCfg<T, true>;
-    if (g.M <= 0 || g.N <= 0) return TRSM_SUCCESS;
+    if (g.M <= 0 || g.N <= 0 || nz <= 0) return TRSM_SUCCESS;
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -24,12 +24,12 @@ static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
     }
-    const int64_t ctas = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
+    const int64_t ctas = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN) * nz;
     if (ctas >= 2 * sms) {
-        const dim3 grid((unsigned)((g.M + C::BM - 1) / C::BM), (unsigned)((g.N + C::BN - 1) / C::BN));
+        const dim3 grid((unsigned)((g.M + C::BM - 1) / C::BM), (unsigned)((g.N + C::BN - 1) / C::BN), (unsigned)nz);
         gemm_kernel<T, false><<<grid, 256, 0, st>>>(g);
     } else {
-        const dim3 grid((unsigned)((g.M + S::BM - 1) / S::BM), (unsigned)((g.N + S::BN - 1) / S::BN));
+        const dim3 grid((unsigned)((g.M + S::BM - 1) / S::BM), (unsigned)((g.N + S::BN - 1) / S::BN), (unsigned)nz);
         gemm_kernel<T, true><<<grid, 256, 0, st>>>(g);
     }
     return launch_status();
@@ -38,7 +38,7 @@ static int gemm_launch(const GemmArgs<T> &g, cudaStream_t st) {
 // Launch the single-precision GEMM with large tiles when they fill at least
 // two waves of the GPU's SMs, else with the small tiles.
 template <typename T>
-static int sp_launch(const SpArgs &g, cudaStream_t st) {
+static int sp_launch(const SpArgs &g, cudaStream_t st, int nz = 1) {
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -47,14 +47,15 @@ static int sp_launch(const SpArgs &g, cudaStream_t st) {
         if (sms <= 0) sms = 152;
     }
     using Big = SpTile<T, false>;
-    const int64_t big_ctas = ((g.M + Big::BM - 1) / Big::BM) * ((g.N + Big::BN - 1) / Big::BN);
+    const int64_t big_ctas = ((g.M + Big::BM - 1) / Big::BM) * ((g.N + Big::BN - 1) / Big::BN) * nz;
     auto go = [&](auto tile_tag, auto kern) -> int {
         using Tl = decltype(tile_tag);
         if (Tl::SMEM > 48 * 1024) {
             const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tl::SMEM);
             if (e != cudaSuccess) return cuda_status(e);
         }
-        const dim3 grid((unsigned)((g.M + Tl::BM - 1) / Tl::BM), (unsigned)((g.N + Tl::BN - 1) / Tl::BN));
+        const dim3 grid((unsigned)((g.M + Tl::BM - 1) / Tl::BM), (unsigned)((g.N + Tl::BN - 1) / Tl::BN),
+                        (unsigned)nz);
         kern<<<grid, 256, Tl::SMEM, st>>>(g);
         return launch_status();
     };
@@ -151,7 +152,7 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    kern<<<dim3(tb, 7), 256, smem, st>>>(L, lda, m, nb, W);
+    kern<<<dim3(tb, 7), 256, smem, st>>>(L, lda, m, nb, W, 0, 0);
     return launch_status();
 }
 
@@ -224,17 +225,17 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
 
     const int64_t tb = (m + nb - 1) / nb;
     if constexpr (std::is_same<T, float>::value) {
-        if (tc_panels && tc_fused_usable(m, n, nb)) {
+        if (tc_panels && !a.tri_rhs && tc_fused_usable(m, n, nb)) {
             // look-ahead form (tc_gemm.cu): every launch but the last is an
             // update with the previous block's apply folded in (phase 2);
             // the last holds the two remaining applies (phase 1)
             timer.begin();
-            TcSide side;
-            rc = tc_side_open(side, st);
-            if (!rc) rc = tc_fused_prepare_side(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, &side);
+            TcSide *side = nullptr;
+            rc = tc_side_acquire(st, &side);
+            if (!rc) rc = tc_fused_prepare_side(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, side);
             for (int64_t t = 0; !rc && t + 1 < tb; ++t)
-                rc = tc_fused_step_side(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, &side);
-            tc_side_close(side);
+                rc = tc_fused_step_side(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, side);
+            tc_side_release(side);
             if (rc || (rc = timer.end(2))) return rc;
             timer.begin();
             rc = tc_fused_step(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
@@ -245,7 +246,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         }
     }
     if constexpr (std::is_same<T, float2>::value) {
-        if (tc_panels && tc_fused_usable_c64(m, n, nb)) {
+        if (tc_panels && !a.tri_rhs && tc_fused_usable_c64(m, n, nb)) {
             // the look-ahead form in real form (tc_gemm.cu), phases as for f32
             timer.begin();
             rc = tc_fused_prepare_c64(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st);
@@ -263,6 +264,10 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     for (int64_t t = 0; t < tb; ++t) {
         const int64_t r0 = t * nb;
         const int64_t mb = (m - r0 < nb) ? m - r0 : nb;
+        // a lower-triangular right-hand side (the identity of the triangular
+        // inverse) has no nonzero column past block t in block rows <= t, so
+        // X_t and this step's update touch only the first (t+1) nb columns
+        const int64_t nt = (a.tri_rhs && (t + 1) * nb < n) ? (t + 1) * nb : n;
         // Phase 1: X_t = gamma * D_t^{-1} R_t into the panel (gamma = alpha at
         // t = 0; later block rows already carry alpha through the updates).
         const T gamma = (t == 0) ? alpha : one;
@@ -270,15 +275,15 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
             // both products on the tensor cores: X_t straight over R_t in B,
             // its split copy straight into the update's operand panels
             const bool has_update = r0 + nb < m;
-            if (tc_panels && tc_apply_usable(mb, n) &&
-                (!has_update || tc_update_usable(m - r0 - nb, n, nb))) {
+            if (tc_panels && tc_apply_usable(mb, nt) &&
+                (!has_update || tc_update_usable(m - r0 - nb, nt, nb))) {
                 timer.begin();
-                rc = tc_apply_f32(mb, n, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
+                rc = tc_apply_f32(mb, nt, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
                 if (rc || (rc = timer.end(1))) return rc;
                 timer.begin();
                 if (has_update) {
                     const T beta = (t == 0) ? alpha : one;
-                    rc = tc_update_f32(m - r0 - nb, n, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
+                    rc = tc_update_f32(m - r0 - nb, nt, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
                                        a.ldb, beta, m, tc_panels, st);
                     if (rc) return rc;
                 }
@@ -289,15 +294,15 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         if constexpr (std::is_same<T, float2>::value) {
             // the same with the complex products in real form
             const bool has_update = r0 + nb < m;
-            if (tc_panels && tc_apply_usable_c64(mb, n) &&
-                (!has_update || tc_update_usable(m - r0 - nb, 2 * n, 2 * nb))) {
+            if (tc_panels && tc_apply_usable_c64(mb, nt) &&
+                (!has_update || tc_update_usable(m - r0 - nb, 2 * nt, 2 * nb))) {
                 timer.begin();
-                rc = tc_apply_c64(mb, n, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
+                rc = tc_apply_c64(mb, nt, W + t * nb * nb, nb, B + r0, a.ldb, gamma, m, tc_panels, has_update, st);
                 if (rc || (rc = timer.end(1))) return rc;
                 timer.begin();
                 if (has_update) {
                     const T beta = (t == 0) ? alpha : one;
-                    rc = tc_update_c64(m - r0 - nb, n, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
+                    rc = tc_update_c64(m - r0 - nb, nt, nb, L + r0 * a.lda + r0 + nb, a.lda, nullptr, 0, B + r0 + nb,
                                        a.ldb, beta, m, tc_panels, st);
                     if (rc) return rc;
                 }
@@ -309,14 +314,14 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         rc = kSpNotApplicable;
         if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
             // R_t (column-major block row of B) -> row-major panel P
-            const dim3 tgrid((unsigned)((mb + 31) / 32), (unsigned)((n + 31) / 32));
-            transpose_kernel<T><<<tgrid, dim3(32, 8), 0, st>>>(B + r0, a.ldb, Pw, ldx, n, mb);
+            const dim3 tgrid((unsigned)((mb + 31) / 32), (unsigned)((nt + 31) / 32));
+            transpose_kernel<T><<<tgrid, dim3(32, 8), 0, st>>>(B + r0, a.ldb, Pw, ldx, nt, mb);
             if ((rc = launch_status())) return rc;
-            rc = apply_sp_launch<T>(mb, n, W + t * nb * nb, nb, Pw, ldx, Xw, gamma, st);
+            rc = apply_sp_launch<T>(mb, nt, W + t * nb * nb, nb, Pw, ldx, Xw, gamma, st);
         }
         if (rc == kSpNotApplicable) {
             GemmArgs<T> ap;
-            ap.M = mb; ap.N = n; ap.K = mb;
+            ap.M = mb; ap.N = nt; ap.K = mb;
             ap.A = W + t * nb * nb; ap.lda = nb;
             ap.B = B + r0; ap.ldb = a.ldb;
             ap.C = Xw; ap.ldc = ldx;
@@ -335,20 +340,167 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         if (r0 + nb < m) {
             const T beta = (t == 0) ? alpha : one;
             const T *Lp = L + r0 * a.lda + r0 + nb;
-            if ((rc = update_launch<T>(m - r0 - nb, n, nb, Lp, a.lda, Xw, ldx, B + r0 + nb, a.ldb, beta,
+            if ((rc = update_launch<T>(m - r0 - nb, nt, nb, Lp, a.lda, Xw, ldx, B + r0 + nb, a.ldb, beta,
                                        minus_one, st, m, tc_panels)))
                 return rc;
         }
         {
             // X_t (row-major panel) back into its block row of B (column-major)
-            const dim3 grid((unsigned)((n + 31) / 32), (unsigned)((mb + 31) / 32));
-            transpose_kernel<T><<<grid, dim3(32, 8), 0, st>>>(Xw, ldx, B + r0, a.ldb, mb, n);
+            const dim3 grid((unsigned)((nt + 31) / 32), (unsigned)((mb + 31) / 32));
+            transpose_kernel<T><<<grid, dim3(32, 8), 0, st>>>(Xw, ldx, B + r0, a.ldb, mb, nt);
             if ((rc = launch_status())) return rc;
         }
         if ((rc = timer.end(2))) return rc;
     }
     if (a.ms)
         for (int q = 0; q < 3; ++q) a.ms[q] = timer.acc[q];
+    return TRSM_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// The blocked path over a strided batch of column-major systems in one
+// sequence of launches: every kernel carries the system index in its grid's
+// last dimension (llama.cpp PR 17457 leaves its 128 x 128 batched case
+// unsupported; one launch sequence serves any batch here).  The inversion
+// runs once per distinct A (once in all when the systems share A, sA == 0);
+// then per block row t one apply X_t = gamma D_t^{-1} R_t, one trailing
+// update and one copy of X_t back into B, each over the whole batch.  The
+// products run on the FMA-pipe kernels (these systems are too small for
+// the tensor-core tiles).  Workspace (256-byte aligned): the inverted blocks
+// (cnt or 1 systems x ceil(m/nb) x nb x nb), then the X_t and R_t panels
+// (cnt x nb x panel_ld(n) each).
+// ---------------------------------------------------------------------------
+template <typename T>
+int blocked_solve_batched_typed(const BatchedBlockedArgs &a, cudaStream_t st) {
+    const int64_t m = a.m, n = a.n, nb = a.nb, cnt = a.batch;
+    if (cnt <= 0) return TRSM_SUCCESS;
+    if (cnt > 65535) return -12;
+    const bool shared_a = a.strideA == 0;
+    const T *L = static_cast<const T *>(a.A);
+    T *B = static_cast<T *>(a.B);
+    T alpha;
+    memcpy(&alpha, a.alpha, sizeof(T));
+    const int64_t tb = (m + nb - 1) / nb;
+    const int64_t ldx = panel_ld(n);
+    const int64_t sW = shared_a ? 0 : tb * nb * nb;  // element stride of the systems' inverted blocks
+    const int64_t sX = nb * ldx;
+    const int nA = shared_a ? 1 : (int)cnt;
+    T *W = static_cast<T *>(a.ws);
+    T *Xw = reinterpret_cast<T *>(static_cast<char *>(a.ws) + round256((int64_t)nA * tb * nb * nb * sizeof(T)));
+    T *Pw = reinterpret_cast<T *>(reinterpret_cast<char *>(Xw) + round256(cnt * sX * (int64_t)sizeof(T)));
+    const int nz = (int)cnt;
+    int rc = TRSM_SUCCESS;
+
+    // Phase 0: every diagonal block of every distinct A
+    auto invert = [&](auto ib_tag) -> int {
+        constexpr int IB = decltype(ib_tag)::value;
+        inv_diag_l1_kernel<T, IB><<<dim3((unsigned)(tb * 8), (unsigned)nA), IB, 0, st>>>(L, a.lda, m, (int)nb, W,
+                                                                                      a.strideA, sW);
+        int r = launch_status();
+        if (r) return r;
+        constexpr size_t smem = inv_offdiag_smem<T, IB>();
+        auto kern = inv_offdiag_kernel<T, IB>;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        kern<<<dim3((unsigned)tb, 7, (unsigned)nA), 256, smem, st>>>(L, a.lda, m, (int)nb, W, a.strideA, sW);
+        return launch_status();
+    };
+    switch (nb) {
+        case 128: rc = invert(std::integral_constant<int, 16>{}); break;
+        case 256: rc = invert(std::integral_constant<int, 32>{}); break;
+        case 512: rc = invert(std::integral_constant<int, 64>{}); break;
+        default: return -9;
+    }
+    if (rc) return rc;
+
+    T one;
+    memset(&one, 0, sizeof(T));
+    reinterpret_cast<typename Elem<T>::Real *>(&one)[0] = 1;
+    T minus_one = one;
+    reinterpret_cast<typename Elem<T>::Real *>(&minus_one)[0] = -1;
+    constexpr bool kSp = std::is_same<T, float>::value || std::is_same<T, float2>::value;
+    const int64_t eb = (int64_t)sizeof(T);
+    // the FMA-pipe single-precision kernels read A in 16-byte chunks
+    const bool sp_ok = kSp && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) && (a.lda * eb) % 16 == 0 &&
+                       (a.strideA * eb) % 16 == 0;
+
+    for (int64_t t = 0; t < tb; ++t) {
+        const int64_t r0 = t * nb;
+        const int64_t mb = (m - r0 < nb) ? m - r0 : nb;
+        const T gamma = (t == 0) ? alpha : one;
+        const T *Wt = W + t * nb * nb;
+        // Phase 1: X_t = gamma D_t^{-1} R_t into the row-major panels
+        rc = kSpNotApplicable;
+        if constexpr (kSp) {
+            const dim3 tgrid((unsigned)((mb + 31) / 32), (unsigned)((n + 31) / 32), (unsigned)nz);
+            transpose_kernel<T><<<tgrid, dim3(32, 8), 0, st>>>(B + r0, a.ldb, Pw, ldx, n, mb, a.strideB, sX);
+            if ((rc = launch_status())) return rc;
+            SpArgs g;
+            g.M = n; g.N = mb; g.K = mb;
+            g.A = Pw; g.lda = ldx; g.sA = sX;
+            g.X = Wt; g.ldx = nb; g.sX = sW;
+            g.C = Xw; g.ldc = ldx; g.sC = sX;
+            g.beta = make_float2(0.f, 0.f);
+            g.gamma = make_float2(0.f, 0.f);
+            memcpy(&g.gamma, &gamma, sizeof(T));
+            g.beta_zero = 1;
+            g.k_by_col = 1;
+            rc = sp_launch<T>(g, st, nz);
+        }
+        if (rc == kSpNotApplicable) {
+            GemmArgs<T> ap;
+            ap.M = mb; ap.N = n; ap.K = mb;
+            ap.A = Wt; ap.lda = nb; ap.sA = sW;
+            ap.B = B + r0; ap.ldb = a.ldb; ap.sB = a.strideB;
+            ap.C = Xw; ap.ldc = ldx; ap.sC = sX;
+            ap.gamma = gamma;
+            ap.beta = one; ap.beta_zero = 1; ap.a_lower = 1;
+            ap.b_rowmajor = 0; ap.c_rowmajor = 1;
+            rc = gemm_launch<T>(ap, st, nz);
+        }
+        if (rc) return rc;
+        // Phase 2: B[r0+nb:, :] = beta B[...] - L[r0+nb:, t-block] X_t
+        if (r0 + nb < m) {
+            const T beta = (t == 0) ? alpha : one;
+            const T *Lp = L + r0 * a.lda + r0 + nb;
+            rc = kSpNotApplicable;
+            if constexpr (kSp) {
+                if (sp_ok && ((reinterpret_cast<uintptr_t>(Lp) & 15) == 0)) {
+                    SpArgs g;
+                    g.M = m - r0 - nb; g.N = n; g.K = nb;
+                    g.A = Lp; g.lda = a.lda; g.sA = a.strideA;
+                    g.X = Xw; g.ldx = ldx; g.sX = sX;
+                    g.C = B + r0 + nb; g.ldc = a.ldb; g.sC = a.strideB;
+                    g.beta = make_float2(0.f, 0.f);
+                    g.gamma = make_float2(0.f, 0.f);
+                    memcpy(&g.beta, &beta, sizeof(T));
+                    memcpy(&g.gamma, &minus_one, sizeof(T));
+                    g.beta_zero = 0;
+                    g.k_by_col = 0;
+                    rc = sp_launch<T>(g, st, nz);
+                }
+            }
+            if (rc == kSpNotApplicable) {
+                GemmArgs<T> up;
+                up.M = m - r0 - nb; up.N = n; up.K = nb;
+                up.A = Lp; up.lda = a.lda; up.sA = a.strideA;
+                up.B = Xw; up.ldb = ldx; up.sB = sX;
+                up.C = B + r0 + nb; up.ldc = a.ldb; up.sC = a.strideB;
+                up.gamma = minus_one;
+                up.beta = beta;
+                up.beta_zero = 0; up.a_lower = 0;
+                up.b_rowmajor = 1; up.c_rowmajor = 0;
+                rc = gemm_launch<T>(up, st, nz);
+            }
+            if (rc) return rc;
+        }
+        // X_t (row-major panels) back into the block rows of B
+        const dim3 grid((unsigned)((n + 31) / 32), (unsigned)((mb + 31) / 32), (unsigned)nz);
+        transpose_kernel<T><<<grid, dim3(32, 8), 0, st>>>(Xw, ldx, B + r0, a.ldb, mb, n, sX, a.strideB);
+        if ((rc = launch_status())) return rc;
+    }
     return TRSM_SUCCESS;
 }
 

@@ -65,6 +65,7 @@ struct SpArgs {
     float2 beta, gamma;  // C = beta*C + gamma*A*X (.x only for real)
     int beta_zero;       // do not read C
     int k_by_col;        // X(k, c) = 0 for k > c: column tile [n0, n0+BN) stops K at n0 + BN
+    int64_t sA = 0, sX = 0, sC = 0;  // grid z: systems of a batch, element strides
 };
 
 // 16-byte copy of src_bytes (0..16) with zero fill of the rest.
@@ -139,9 +140,9 @@ __global__ void __launch_bounds__(256) sp_update_kernel(const SpArgs g) {
     E *As = reinterpret_cast<E *>(smem_raw);                      // [STAGES][BK][BM]
     E *Xs = As + STAGES * Tl::A_STAGE;                            // [STAGES][BK][BN]
 
-    const E *A = static_cast<const E *>(g.A);
-    const E *X = static_cast<const E *>(g.X);
-    E *Cm = static_cast<E *>(g.C);
+    const E *A = static_cast<const E *>(g.A) + (int64_t)blockIdx.z * g.sA;
+    const E *X = static_cast<const E *>(g.X) + (int64_t)blockIdx.z * g.sX;
+    E *Cm = static_cast<E *>(g.C) + (int64_t)blockIdx.z * g.sC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wm = warp & 1, wn = warp >> 1;
     const int lx = lane & 7, ly = lane >> 3;

@@ -57,6 +57,9 @@ struct BlockedArgs {
     alignas(16) unsigned char alpha[16];
     void *ws;        // >= blocked_workspace_bytes(elem, m, n, nb), 256-byte aligned
     float *ms;       // optional: per-phase milliseconds (profiling entry)
+    // B holds the identity (alpha = 1): block row t's solve and update touch
+    // only its first (t+1) nb columns (the triangular inverse)
+    bool tri_rhs = false;
 };
 
 // Bytes of workspace the blocked path needs: the inverted diagonal blocks
@@ -121,15 +124,55 @@ int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t 
 // kernels), and its value (synchronises the device).
 int device_status_word(int **out);
 int device_status(int clear);
+// Polls of the first bounded wait on each item of the batched f32 small
+// kernel: the compiled limit unless trsm_set_wait_limit lowered it.
+uint32_t first_wait_limit();
+int set_first_wait_limit(int64_t polls);
+
+// Blocked path over a strided batch of column-major systems, one launch
+// sequence for all of them (blocked_launch.cuh); batch <= 65535 (the grid's
+// system dimension), strideA = 0 for one A shared by every system.
+struct BatchedBlockedArgs {
+    int64_t m, n, nb;
+    const void *A;
+    int64_t lda, strideA;
+    void *B;
+    int64_t ldb, strideB;
+    int64_t batch;
+    alignas(16) unsigned char alpha[16];
+    void *ws;  // >= batched_workspace_bytes(...), 256-byte aligned
+};
+inline size_t batched_workspace_bytes(int dtype, int64_t m, int64_t n, int64_t nb, int64_t batch, bool shared_a) {
+    const int64_t eb = dtype == 0 ? 4 : dtype == 3 ? 16 : 8;
+    const int64_t tb = (m + nb - 1) / nb;
+    return (size_t)(round256((shared_a ? 1 : batch) * tb * nb * nb * eb) + 2 * round256(batch * nb * panel_ld(n) * eb));
+}
+int blocked_solve_batched_f32(const BatchedBlockedArgs &a, cudaStream_t st);
+int blocked_solve_batched_f64(const BatchedBlockedArgs &a, cudaStream_t st);
+int blocked_solve_batched_c64(const BatchedBlockedArgs &a, cudaStream_t st);
+int blocked_solve_batched_c128(const BatchedBlockedArgs &a, cudaStream_t st);
 
 int blocked_solve_f32(const BlockedArgs &a, cudaStream_t st);
 int blocked_solve_f64(const BlockedArgs &a, cudaStream_t st);
 int blocked_solve_c64(const BlockedArgs &a, cudaStream_t st);
 int blocked_solve_c128(const BlockedArgs &a, cudaStream_t st);
 
+// The dispatch behind every solve entry point, after argument checks: alpha
+// = 0, the small regime (m <= 64), batches of m = 128 systems, the blocked
+// path.  ws / ws_bytes: the blocked path's workspace (plus the transposed
+// copies of row-major systems); when it is missing or too small the call
+// allocates one with cudaMallocAsync on st if may_alloc, else returns
+// TRSM_ERR_WORKSPACE before launching anything.  nb = 0: the table's block
+// size.  ms: optional phase times (synchronises st).
+int solve_dispatch(int dtype, int layout, int64_t m, int64_t n, const void *alpha, const void *A, int64_t lda,
+                   int64_t sA, void *B, int64_t ldb, int64_t sB, int64_t batch, int64_t nb, void *ws,
+                   size_t ws_bytes, bool may_alloc, cudaStream_t st, float *ms, bool tri_rhs = false);
+
 // Row-major <-> column-major copy of a rows x cols matrix (out-of-place),
 // used to run row-major inputs through the column-major blocked path.
+// With nz > 1: nz such copies, src and dst advancing by s_src / s_dst elements.
 int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
-                          int64_t rows, int64_t cols, cudaStream_t st);
+                          int64_t rows, int64_t cols, cudaStream_t st, int64_t s_src = 0, int64_t s_dst = 0,
+                          int nz = 1);
 
 }  // namespace trsm

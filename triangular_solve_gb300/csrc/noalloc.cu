@@ -10,11 +10,15 @@
 // the file-scope device array below, of fixed size; every GPU that loads the
 // library holds that array until the process exits.
 //
-// Set-up: the first call on a device looks up the array's device address
-// with cudaGetSymbolAddress (with that device current) and caches it; make
-// that first call before any stream capture.  In host code the array's name
-// is only a host-side stand-in, never a device address, which is why the
-// looked-up pointer is what the kernels receive.
+// Set-up: the first call on a device that reaches the blocked path looks up
+// the array's device address with cudaGetSymbolAddress (with that device
+// current) and caches it; make that first call before any stream capture.
+// In host code the array's name is only a host-side stand-in, never a device
+// address, which is why the looked-up pointer is what the kernels receive.
+// The cached address belongs to the device's primary context: resetting the
+// device (cudaDeviceReset) between calls is not supported.  The f32 blocked
+// path also keeps one side stream and a few events per (device, caller
+// stream), created by the first call that needs them (no device memory).
 //
 // Sharing: every call on a device uses the same array and it keeps the last
 // call's contents.  Nothing in it needs to start at zero: each call writes
@@ -98,51 +102,19 @@ extern "C" int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const
     if (!B || !aligned_to(B, eb)) return -7;
     if (m <= 64 && n > 64LL * 65535) return -3;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SmallArgs s;
-    s.m = m; s.n = n; s.layout = TRSM_COL_MAJOR;
-    s.A = A; s.lda = lda; s.strideA = 0;
-    s.B = B; s.ldb = ldb; s.strideB = 0;
-    s.batch = 1;
-    memset(s.alpha, 0, sizeof(s.alpha));
-    memcpy(s.alpha, alpha, (size_t)eb);
-
-    if (zero) {
-        switch (dtype) {
-            case TRSM_F32: return launch_zero_f32(s, st);
-            case TRSM_F64: return launch_zero_f64(s, st);
-            case TRSM_C64: return launch_zero_c64(s, st);
-            default: return launch_zero_c128(s, st);
-        }
-    }
-    if (m <= 64) {  // the small regime needs no scratch
-        const bool rowlane = n <= 8;
-        switch (dtype) {
-            case TRSM_F32: return rowlane ? launch_rowlane_f32(s, st) : launch_colreg_f32(s, st);
-            case TRSM_F64: return rowlane ? launch_rowlane_f64(s, st) : launch_colreg_f64(s, st);
-            case TRSM_C64: return rowlane ? launch_rowlane_c64(s, st) : launch_colreg_c64(s, st);
-            default: return rowlane ? launch_rowlane_c128(s, st) : launch_colreg_c128(s, st);
-        }
-    }
-
-    const int nb = trsm_llnn_select_nb(dtype, m, n);  // the table's block size, as trsm_llnn uses
-    const size_t need = blocked_workspace_bytes((int)dtype, m, n, nb);
-    if (need > (size_t)TRSM_NOALLOC_SCRATCH_BYTES) return TRSM_ERR_WORKSPACE;
+    // Only the blocked path (m > 64) reads a workspace; its size with the
+    // table's block size decides up front whether the array can hold it.
     void *scratch = nullptr;
-    const int rc = scratch_on_current_device(&scratch);
-    if (rc != TRSM_SUCCESS) return rc;
-
-    BlockedArgs ba;
-    ba.m = m; ba.n = n; ba.nb = nb;
-    ba.A = A; ba.lda = lda;
-    ba.B = B; ba.ldb = ldb;
-    memcpy(ba.alpha, s.alpha, sizeof(ba.alpha));
-    ba.ws = scratch;
-    ba.ms = nullptr;
-    switch (dtype) {
-        case TRSM_F32: return blocked_solve_f32(ba, st);
-        case TRSM_F64: return blocked_solve_f64(ba, st);
-        case TRSM_C64: return blocked_solve_c64(ba, st);
-        default: return blocked_solve_c128(ba, st);
+    if (m > 64 && !zero) {
+        const int nb = trsm_llnn_select_nb(dtype, m, n);
+        if (blocked_workspace_bytes((int)dtype, m, n, nb) > (size_t)TRSM_NOALLOC_SCRATCH_BYTES)
+            return TRSM_ERR_WORKSPACE;
+        const int rc = scratch_on_current_device(&scratch);
+        if (rc != TRSM_SUCCESS) return rc;
     }
+    // The same dispatch as trsm_llnn, with the array as the workspace and
+    // allocation switched off: both entry points pick the same kernels.
+    return solve_dispatch((int)dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, 0, scratch,
+                          scratch ? (size_t)TRSM_NOALLOC_SCRATCH_BYTES : 0, /*may_alloc=*/false,
+                          static_cast<cudaStream_t>(stream), nullptr);
 }

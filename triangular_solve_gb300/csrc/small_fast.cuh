@@ -609,7 +609,8 @@ __device__ __forceinline__ bool unit_any(int unit, int nthreads, bool flag) {
 template <int M, int WPI>
 __global__ void __launch_bounds__(TmaUnits<WPI>::kThreads, 1)
     small_tma_f32_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                         const int n, const float alpha, const int64_t items, int *status) {
+                         const int n, const float alpha, const int64_t items, int *status,
+                         const uint32_t wait_limit) {
     using S = SwzStage<M>;
     constexpr int NR = S::NR, UNITS = TmaUnits<WPI>::kUnits, UT = 32 * WPI, CPT = 2 / WPI;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -648,7 +649,10 @@ __global__ void __launch_bounds__(TmaUnits<WPI>::kThreads, 1)
             bulk_wait_read<0>();  // the last item's stores have read stage s^1
             issue(item + step, s ^ 1);
         }
-        const bool ok = mbar_wait(smem_u32(&full_bar[unit][s]), (uint32_t)(it >> 1) & 1u);
+        // wait_limit polls (kWaitLimit unless lowered through
+        // trsm_set_wait_limit); the waits that drain the copies in flight
+        // below keep the full limit
+        const bool ok = mbar_wait_n(smem_u32(&full_bar[unit][s]), (uint32_t)(it >> 1) & 1u, wait_limit);
         if (unit_any(unit, UT, !ok)) {
             // a copy never completed: report, let the copies in flight land, stop
             if (leader) record_timeout(status);
@@ -869,7 +873,8 @@ static int launch_tma_f32(const SmallGeom &g, float alpha, cudaStream_t st) {
     const int64_t items = g.batch * ((g.n + 63) / 64);
     int64_t ctas = (items + UNITS - 1) / UNITS;
     if (ctas > sms) ctas = sms;  // persistent: one CTA per SM
-    kern<<<(unsigned)ctas, TmaUnits<WPI>::kThreads, smem, st>>>(ma, mb, g.n, alpha, items, status);
+    kern<<<(unsigned)ctas, TmaUnits<WPI>::kThreads, smem, st>>>(ma, mb, g.n, alpha, items, status,
+                                                                 first_wait_limit());
     return launch_status();
 }
 

@@ -1,7 +1,10 @@
 // Host side of the tensor-core f32 trailing update: TF32 head/tail split of
 // the two panels, tensor maps for the TMA loads, launch, and the device
 // status word that the kernels' bounded waits report to.
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -520,27 +523,72 @@ size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb) {
 // and the inverted blocks only) run beside the launch before the one that
 // needs them.  launched[t & 1] marks launch t done, split[b & 1] block b's
 // operands ready; the side stream starts after everything already on st.
-int tc_side_open(TcSide &side, cudaStream_t st) {
-    cudaError_t e = cudaStreamCreateWithFlags(&side.s, cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-        e = cudaEventCreateWithFlags(&side.launched[i], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.split[i], cudaEventDisableTiming);
-    }
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.start, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventRecord(side.start, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.start, 0);
-    return cuda_status(e);
-}
+namespace {
 
-void tc_side_close(TcSide &side) {
-    // released once their pending work is done
+// One side stream and its events per (device, caller stream), created on
+// first use and kept for the life of the process; a solve holds its slot
+// (the lock) from acquire to release, so the event records of two solves
+// never interleave.  Reuse across solves is safe: every wait of a solve
+// refers to an event recorded earlier in the same solve.
+struct SideSlot : TcSide {
+    std::mutex mu;
+};
+std::mutex g_side_map_mu;
+std::map<std::pair<int, cudaStream_t>, SideSlot *> g_side_slots;
+
+void side_destroy(TcSide &side) {
     for (int i = 0; i < 2; ++i) {
         if (side.launched[i]) cudaEventDestroy(side.launched[i]);
         if (side.split[i]) cudaEventDestroy(side.split[i]);
     }
     if (side.start) cudaEventDestroy(side.start);
     if (side.s) cudaStreamDestroy(side.s);
-    side = TcSide();
+    side.s = nullptr;
+    side.launched[0] = side.launched[1] = side.split[0] = side.split[1] = side.start = nullptr;
+}
+
+}  // namespace
+
+int tc_side_acquire(cudaStream_t st, TcSide **out) {
+    *out = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    SideSlot *slot = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_side_map_mu);
+        SideSlot *&p = g_side_slots[{dev, st}];
+        if (!p) p = new SideSlot;
+        slot = p;
+    }
+    slot->mu.lock();
+    TcSide &side = *slot;
+    if (!side.s) {
+        e = cudaStreamCreateWithFlags(&side.s, cudaStreamNonBlocking);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&side.launched[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.split[i], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&side.start, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            side_destroy(side);
+            slot->mu.unlock();
+            return cuda_status(e);
+        }
+    }
+    // the side stream starts after everything already queued on st
+    e = cudaEventRecord(side.start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.start, 0);
+    if (e != cudaSuccess) {
+        slot->mu.unlock();
+        return cuda_status(e);
+    }
+    *out = &side;
+    return TRSM_SUCCESS;
+}
+
+void tc_side_release(TcSide *side) {
+    if (side) static_cast<SideSlot *>(side)->mu.unlock();
 }
 
 // W_0 = L_panel_0 D_0^-1 and the split of R_0, before step 0; block 1's W
@@ -767,6 +815,18 @@ int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 
                                          f.d0_lo, st)))
         return rc;
     return tc_launch(P, np, st);
+}
+
+namespace {
+std::atomic<uint32_t> g_first_wait_limit{kWaitLimit};
+}  // namespace
+
+uint32_t first_wait_limit() { return g_first_wait_limit.load(std::memory_order_relaxed); }
+
+int set_first_wait_limit(int64_t polls) {
+    g_first_wait_limit.store(polls < 0 || polls > (int64_t)kWaitLimit ? kWaitLimit : (uint32_t)polls,
+                             std::memory_order_relaxed);
+    return TRSM_SUCCESS;
 }
 
 int device_status(int clear) {

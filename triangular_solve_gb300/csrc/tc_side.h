@@ -19,8 +19,12 @@ struct TcSide {
     cudaEvent_t launched[2] = {nullptr, nullptr}, split[2] = {nullptr, nullptr}, start = nullptr;
 };
 
-int tc_side_open(TcSide &side, cudaStream_t st);
-void tc_side_close(TcSide &side);  // resources released once their pending work is done
+// The side stream and events of (current device, st): created by the first
+// call for that pair and kept for the life of the process (no device
+// memory).  The caller holds them until tc_side_release; the side stream
+// starts after everything already queued on st.
+int tc_side_acquire(cudaStream_t st, TcSide **side);
+void tc_side_release(TcSide *side);
 // tc_fused_prepare / tc_fused_step with the side stream (nullptr: none)
 int tc_fused_prepare_side(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
                           const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side);
