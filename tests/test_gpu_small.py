@@ -197,3 +197,36 @@ def test_fp64_few_systems_spread_columns(env, dtype, m, n, batch):
     L, B = ti.generate(dtype, m, n, batch, kind="dd64", seed=m * n + batch)
     alpha = (0.75 + 0.5j) if ti.IS_COMPLEX[dtype] else 0.75
     _parity(env, dtype, L, B, alpha, f"spread {dtype} m={m} n={n} batch={batch}")
+
+
+@pytest.mark.parametrize("m,n,batch", [(64, 64, 700), (64, 40, 400), (64, 100, 350), (48, 64, 612), (32, 64, 900),
+                                       (64, 32, 700), (48, 17, 500), (32, 30, 800)])
+def test_persistent_c64_path_many_items(env, m, n, batch):
+    """Enough (system, column-slice) items for the persistent complex64 TMA
+    kernel: 64-column slices (a warp pair per item) and, for n <= 32,
+    32-column slices (a warp per item); ragged last slices, complex alpha,
+    NaN in the upper triangle."""
+    L, B = ti.generate("c64", m, n, batch, kind="dd64", seed=3 * m + n)
+    _parity(env, "c64", L, B, 0.5 - 0.75j, f"c64 tma m={m} n={n} batch={batch}")
+    assert env["tg"].trsm_device_status() == 0
+
+
+@pytest.mark.parametrize("m", [32, 48, 64])
+@pytest.mark.parametrize("geom", ["padded", "gaps", "shared_a"])
+def test_persistent_c64_strided_layouts(env, m, geom):
+    """The complex64 TMA kernel on layouts its tensor maps must describe:
+    padded leading dimensions, gaps between systems, one shared L."""
+    n, batch = 64, 700
+    L, B = ti.generate("c64", m, n, batch, kind="dd64", seed=m + 1)
+    if geom == "shared_a":
+        L[:] = L[0]
+        a, b, geo = storage_pair(L[:1], B)
+        geo["batch"], geo["sa"] = batch, 0
+        b = ti.to_storage(B, "col")
+        raw = gpu_solve_buffers("c64", a, b, geo, 1.0, env["torch"], env["tg"])
+        ref = oracle_buffers("c64", a, b, geo, 1.0, env["oracle"])
+        assert_parity("c64", logical(raw, geo), logical(ref, geo), f"shared A m={m}")
+    else:
+        kw = dict(lda=m + 2, ldb=m + 4) if geom == "padded" else dict(stride_a=m * m + 32, stride_b=m * n + 16)
+        _parity(env, "c64", L, B, 1.0, f"{geom} m={m}", **kw)
+    assert env["tg"].trsm_device_status() == 0
