@@ -165,117 +165,135 @@ template <int M, int W, int ST>
 __global__ void __launch_bounds__(C64Units<M, W, ST>::kThreads, 1)
     small_tma_c64_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                          const int n, const float2 alpha, const int64_t items, int *status) {
+    static_assert(ST == 1, "one region per unit, refilled chunk by chunk");
     using S = C64Stage<M, W>;
     constexpr int NR = S::NR, UNITS = C64Units<M, W, ST>::kUnits, UT = W;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[UNITS][ST];
+    // per unit and 16-row block J: barL[J] = column block J of L (blocks
+    // (J..NR-1, J)), barB[J] = right-hand-side box J; each completes once per item
+    __shared__ __align__(8) uint64_t barL[UNITS][NR], barB[UNITS][NR];
     const int tid = threadIdx.x;
     const int unit = tid / UT, pt = tid % UT;  // pt: this thread's column of the slice
     const bool leader = pt == 0;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;  // the swizzle pattern repeats every 1024 bytes
-    float *my = reinterpret_cast<float *>(smem_raw + (sbase - raw)) + unit * ST * S::kElems;
-    if (tid < ST * UNITS) mbar_init(smem_u32(&full_bar[tid / ST][tid % ST]), 1);
+    float *cur = reinterpret_cast<float *>(smem_raw + (sbase - raw)) + unit * S::kElems;
+    float *dinv = cur + S::dinv();
+    if (tid < UNITS * NR) {
+        mbar_init(smem_u32(&barL[tid / NR][tid % NR]), 1);
+        mbar_init(smem_u32(&barB[tid / NR][tid % NR]), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncthreads();
 
     const int slices = (n + W - 1) / W;
-    auto issue = [&](int64_t item, int s) {  // the unit's leader
-        const int sys = (int)(item / slices);
-        const int j0 = (int)(item - (int64_t)sys * slices) * W;
-        const uint32_t bar = smem_u32(&full_bar[unit][s]);
-        const uint32_t st = smem_u32(my + s * S::kElems);
-        mbar_expect_tx(bar, S::kLoadBytes);
-        for (int rb = 0; rb < NR; ++rb)
-            for (int cb = 0; cb <= rb; ++cb)
-                tma_load_3d(st + 4u * (uint32_t)S::lbox(rb, cb), &mapA, 32 * rb, 16 * cb, sys, bar);
-        for (int rb = 0; rb < NR; ++rb) tma_load_3d(st + 4u * (uint32_t)S::bbox(rb), &mapB, 32 * rb, j0, sys, bar);
+    auto coords = [&](int64_t item, int &sys, int &j0) {
+        sys = (int)(item / slices);
+        j0 = (int)(item - (int64_t)sys * slices) * W;
+    };
+    // the unit's leader: column block J of L, and right-hand-side box J
+    auto issue_l = [&](int64_t item, int J) {
+        int sys, j0;
+        coords(item, sys, j0);
+        const uint32_t bar = smem_u32(&barL[unit][J]);
+        mbar_expect_tx(bar, (uint32_t)(NR - J) * 2048u);
+        for (int rb = J; rb < NR; ++rb)
+            tma_load_3d(smem_u32(cur + S::lbox(rb, J)), &mapA, 32 * rb, 16 * J, sys, bar);
+    };
+    auto issue_b = [&](int64_t item, int J) {
+        int sys, j0;
+        coords(item, sys, j0);
+        const uint32_t bar = smem_u32(&barB[unit][J]);
+        mbar_expect_tx(bar, (uint32_t)S::kBBox * 4u);
+        tma_load_3d(smem_u32(cur + S::bbox(J)), &mapB, 32 * J, j0, sys, bar);
     };
     const bool alpha_one = alpha.x == 1.f && alpha.y == 0.f;
-    const f32x2 ar = dup2(alpha.x), ai = dup2(alpha.y), nai = dup2(-alpha.y);
+    const f32x2 ar = dup2(alpha.x), ai = dup2(alpha.y), nai = dup2(-alpha.y), one2 = dup2(1.f);
+    // phases armed (leader) and observed (every thread) per barrier
+    uint32_t armL[NR], armB[NR], seenL[NR], seenB[NR];
+#pragma unroll
+    for (int J = 0; J < NR; ++J) armL[J] = armB[J] = seenL[J] = seenB[J] = 0;
 
     int64_t item = (int64_t)blockIdx.x * UNITS + unit;
     const int64_t step = (int64_t)gridDim.x * UNITS;
-    if (leader && item < items) issue(item, 0);
-    for (int it = 0; item < items; ++it, item += step) {
-        const int s = it % ST;
-        const uint32_t parity = (uint32_t)(it / ST) & 1u;  // uses of stage s before this one
+    if (leader && item < items) {
+#pragma unroll
+        for (int J = 0; J < NR; ++J) {
+            issue_l(item, J);
+            issue_b(item, J);
+            ++armL[J];
+            ++armB[J];
+        }
+    }
+    const int sw = pt & 7;
+    bool failed = false;
+    for (; item < items && !failed; item += step) {
         const bool more = item + step < items;
-        if constexpr (ST == 2) {
-            if (leader && more) {
-                bulk_wait_read<0>();  // the last item's stores have read the other stage
-                issue(item + step, s ^ 1);
-            }
-        }
-        const bool ok = mbar_wait(smem_u32(&full_bar[unit][s]), parity);
-        if (unit_any(unit, UT, !ok)) {
-            // a copy never completed: report, let the copies in flight land, stop
-            if (leader) record_timeout(status);
-            mbar_wait(smem_u32(&full_bar[unit][s]), parity);
-            if constexpr (ST == 2) {
-                if (more) mbar_wait(smem_u32(&full_bar[unit][s ^ 1]), (uint32_t)((it + 1) / ST) & 1u);
-            }
-            break;
-        }
-        float *cur = my + s * S::kElems;
-        float *dinv = cur + S::dinv();
-
-        // L lines to planar form, in place: 8 threads per line, thread q
-        // holding complex rows 2q and 2q+1; the thread that holds a diagonal
-        // entry also writes its reciprocal
-        for (int line = pt / 8; line < 16 * S::kLBoxes; line += UT / 8) {
-            const int q = pt % 8, box = line / 16, c = line % 16;
-            float *ln = cur + box * 512 + c * 32;
-            const float4 v = *reinterpret_cast<const float4 *>(ln + 4 * q);
-            __syncwarp();
-            *reinterpret_cast<float2 *>(ln + 2 * q) = make_float2(v.x, v.z);
-            *reinterpret_cast<float2 *>(ln + 16 + 2 * q) = make_float2(v.y, v.w);
-            // diagonal blocks are boxes rb(rb+3)/2; row c of column c
-            int rb = 0;
-            while (rb < NR - 1 && rb * (rb + 3) / 2 < box) ++rb;
-            if (rb * (rb + 3) / 2 == box && (c >> 1) == q) {
-                const float2 dr = (c & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
-                *reinterpret_cast<float2 *>(dinv + 2 * (16 * rb + c)) = recip(dr);
-            }
-            __syncwarp();
-        }
-        unit_sync(unit, UT);
-
-        // the whole column in registers, 16-row chunk by chunk; right-looking:
-        // once chunk J is solved, its columns update every later chunk, so
-        // each rolled step over k carries (NR-1-J) x 64 independent FMAs
-        const int sw = pt & 7;
+        // accumulators: chunk R collects -sum_J L_RJ X_J; alpha B_R joins it
+        // when chunk R is solved, so box R is needed only from then on
         f32x2 br[NR][8], bi[NR][8];
 #pragma unroll
-        for (int R = 0; R < NR; ++R) {
-            const float *bcol = cur + S::bbox(R) + pt * 32;  // this thread's line of RHS box R
+        for (int R = 0; R < NR; ++R)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) br[R][q] = bi[R][q] = 0ull;
+#pragma unroll
+        for (int J = 0; J < NR; ++J) {
+            if (failed) continue;
+            const bool okl = mbar_wait(smem_u32(&barL[unit][J]), seenL[J] & 1u);
+            const bool okb = okl && mbar_wait(smem_u32(&barB[unit][J]), seenB[J] & 1u);
+            if (unit_any(unit, UT, !okb)) {
+                failed = true;
+                continue;
+            }
+            ++seenL[J];
+            ++seenB[J];
+            // column block J of L to planar lines, in place (8 threads per line,
+            // thread q holding complex rows 2q, 2q+1); the diagonal block's
+            // reciprocals on the way
+            for (int line = pt / 8; line < 16 * (NR - J); line += UT / 8) {
+                const int q = pt % 8, rb = J + line / 16, c = line % 16;
+                float *ln = cur + S::lbox(rb, J) + c * 32;
+                const float4 v = *reinterpret_cast<const float4 *>(ln + 4 * q);
+                __syncwarp();
+                *reinterpret_cast<float2 *>(ln + 2 * q) = make_float2(v.x, v.z);
+                *reinterpret_cast<float2 *>(ln + 16 + 2 * q) = make_float2(v.y, v.w);
+                if (rb == J && (c >> 1) == q) {
+                    const float2 dr = (c & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+                    *reinterpret_cast<float2 *>(dinv + 2 * (16 * J + c)) = recip(dr);
+                }
+                __syncwarp();
+            }
+            unit_sync(unit, UT);
+            // chunk J: alpha B_J + accumulated updates, then its diagonal block
+            float *bcol = cur + S::bbox(J) + pt * 32;  // this thread's line of box J
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 v = *reinterpret_cast<const float4 *>(bcol + 4 * (q ^ sw));
-                br[R][q] = pack2(v.x, v.z);
-                bi[R][q] = pack2(v.y, v.w);
-            }
-            if (!alpha_one) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const f32x2 r = br[R][q], i = bi[R][q];
-                    br[R][q] = ffma2(i, nai, ffma2(r, ar, 0ull));
-                    bi[R][q] = ffma2(r, ai, ffma2(i, ar, 0ull));
+                const f32x2 r = pack2(v.x, v.z), i = pack2(v.y, v.w);
+                if (alpha_one) {
+                    br[J][q] = ffma2(r, one2, br[J][q]);
+                    bi[J][q] = ffma2(i, one2, bi[J][q]);
+                } else {
+                    br[J][q] = ffma2(i, nai, ffma2(r, ar, br[J][q]));
+                    bi[J][q] = ffma2(r, ai, ffma2(i, ar, bi[J][q]));
                 }
             }
-        }
-#pragma unroll
-        for (int J = 0; J < NR; ++J) {
             C64Diag<0>::run(cur + S::lbox(J, J), dinv + 32 * J, br[J], bi[J]);
-            // the solved chunk back over its RHS rows (X out, and x for the
-            // updates below)
-            float *bcol = cur + S::bbox(J) + pt * 32;
+            // X chunk J over box J: it leaves from there, and feeds the updates
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 float r0, r1, i0, i1;
                 unpack2(br[J][q], r0, r1);
                 unpack2(bi[J][q], i0, i1);
                 *reinterpret_cast<float4 *>(bcol + 4 * (q ^ sw)) = make_float4(r0, i0, r1, i1);
+            }
+            fence_proxy_async_smem();
+            unit_sync(unit, UT);
+            if (leader) {
+                int sys, j0;
+                coords(item, sys, j0);
+                tma_store_3d(&mapB, 32 * J, j0, sys, smem_u32(cur + S::bbox(J)));
+                bulk_commit();
             }
             if (J + 1 < NR) {
 #pragma unroll 1
@@ -286,19 +304,31 @@ __global__ void __launch_bounds__(C64Units<M, W, ST>::kThreads, 1)
                         c64_col_update2(cur + S::lbox(R, J) + k * 32, x, br[R], bi[R]);
                 }
             }
-        }
-        fence_proxy_async_smem();
-        unit_sync(unit, UT);
-        if (leader) {
-            const int sys = (int)(item / slices);
-            const int j0 = (int)(item - (int64_t)sys * slices) * W;
-            for (int rb = 0; rb < NR; ++rb) tma_store_3d(&mapB, 32 * rb, j0, sys, smem_u32(cur + S::bbox(rb)));
-            bulk_commit();
-            if constexpr (ST == 1) {
-                if (more) {
-                    bulk_wait_read<0>();  // the stores have read the stage: refill it
-                    issue(item + step, 0);
+            unit_sync(unit, UT);  // column block J and box J are read by every thread
+            if (leader && more) {
+                issue_l(item + step, J);  // the next item's column block J
+                ++armL[J];
+                if (J >= 1) {
+                    bulk_wait_read<1>();  // the store of box J-1 has read it
+                    issue_b(item + step, J - 1);
+                    ++armB[J - 1];
                 }
+            }
+        }
+        if (!failed && leader && more) {
+            bulk_wait_read<0>();
+            issue_b(item + step, NR - 1);
+            ++armB[NR - 1];
+        }
+    }
+    if (failed) {
+        // a copy never completed: report, let every copy in flight land, stop
+        if (leader) {
+            record_timeout(status);
+#pragma unroll
+            for (int J = 0; J < NR; ++J) {
+                for (uint32_t p = seenL[J]; p < armL[J]; ++p) mbar_wait(smem_u32(&barL[unit][J]), p & 1u);
+                for (uint32_t p = seenB[J]; p < armB[J]; ++p) mbar_wait(smem_u32(&barB[unit][J]), p & 1u);
             }
         }
     }
@@ -342,12 +372,9 @@ static int launch_tma_c64_mw(const SmallArgs &a, cudaStream_t st) {
     return launch_status();
 }
 
-// Two stages per unit when that still leaves six or more warps on the SM,
-// else one stage and twice the units.
 template <int M, int W>
 static int launch_tma_c64_m(const SmallArgs &a, cudaStream_t st) {
-    constexpr bool kTwo = C64Units<M, W, 2>::kUnits * (W / 32) >= 6;
-    return launch_tma_c64_mw<M, W, kTwo ? 2 : 1>(a, st);
+    return launch_tma_c64_mw<M, W, 1>(a, st);
 }
 
 inline int launch_tma_c64(const SmallArgs &a, cudaStream_t st) {
