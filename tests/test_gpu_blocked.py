@@ -174,6 +174,21 @@ def test_narrow_path_large(env, dtype):
     assert_parity(dtype, xg, xr, f"narrow {dtype} m={m}")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("m,n", [(513, 1), (640, 8), (1000, 2), (2049, 5), (4096, 3)])
+def test_few_rhs_persistent_path(env, dtype, m, n):
+    """n <= 8 with 16-byte aligned columns of L: the persistent few-right-hand-
+    side kernel (one CTA per 128-row block row, flags between them), ragged
+    last block rows, complex alpha, padded leading dimensions; the device
+    status word stays clear."""
+    pad = {"f32": 4, "f64": 2, "c64": 2, "c128": 1}[dtype]  # keeps every column 16-byte aligned
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + 31 * n)
+    alpha = (0.5 + 1.25j) if ti.IS_COMPLEX[dtype] else -1.25
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, 0, lda=m + pad, ldb=m + 3)
+    assert env["tg"].trsm_device_status() == 0
+    assert_parity(dtype, xg, xr, f"few-rhs {dtype} m={m} n={n}")
+
+
 @pytest.mark.parametrize("m,n,nb,ld_pad", [
     (512, 256, 256, 0),    # two blocks: one update, then both applies in one launch
     (528, 257, 256, 1),    # 16-row last block, one column past a tile, odd ldb (scalar splits)

@@ -4,6 +4,7 @@
 #include <type_traits>
 
 #include "blocked_kernels.cuh"
+#include "few_rhs.cuh"
 #include "gemm_sp.cuh"
 #include "internal.h"
 #include "tc_side.h"
@@ -156,6 +157,67 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
     return launch_status();
 }
 
+// The few-right-hand-sides path (few_rhs.cuh): n <= kFewMaxN columns of a
+// column-major system of order m > kFewMinM, 16-byte aligned L columns, and
+// its data -- the inverted 128-row diagonal blocks, then one flag per block
+// row -- within the blocked path's workspace of ws_bytes.
+constexpr int64_t kFewMinM = 512;
+inline size_t few_rhs_bytes(int64_t m, int elem_bytes) {
+    const int64_t tb = (m + kFewNB - 1) / kFewNB;
+    return (size_t)(round256(tb * kFewNB * kFewNB * elem_bytes) + round256(tb * 4));
+}
+
+template <typename T>
+static bool few_rhs_usable(int64_t m, int64_t n, const T *L, int64_t lda, size_t ws_bytes) {
+    return n >= 1 && n <= kFewMaxN && m > kFewMinM && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) &&
+           (lda * (int64_t)sizeof(T)) % 16 == 0 && few_rhs_bytes(m, (int)sizeof(T)) <= ws_bytes;
+}
+
+// The inversion of the 128-row diagonal blocks, then the persistent kernel
+// (a cooperative launch: its CTAs wait on one another's flags, so all of them
+// must be resident at once).
+template <typename T>
+static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, int64_t ldb, T alpha, void *ws,
+                         cudaStream_t st, float *inv_ms, float *solve_ms) {
+    const int64_t tb = (m + kFewNB - 1) / kFewNB;
+    T *W = static_cast<T *>(ws);
+    int *flags = reinterpret_cast<int *>(static_cast<char *>(ws) + round256(tb * kFewNB * kFewNB * (int64_t)sizeof(T)));
+    cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
+    if (inv_ms)
+        for (auto &x : e) cudaEventCreate(&x);
+    if (inv_ms) cudaEventRecord(e[0], st);
+    int rc = invert_diagonal_blocks<T, kFewNB / 8>(L, lda, m, kFewNB, W, st);
+    if (!rc) rc = cuda_status(cudaMemsetAsync(flags, 0, (size_t)tb * sizeof(int), st));
+    int *status = nullptr;
+    if (!rc) rc = device_status_word(&status);
+    if (inv_ms) cudaEventRecord(e[1], st);
+    constexpr size_t smem = few_rhs_smem<T>();
+    auto kern = few_rhs_kernel<T>;
+    if (!rc) rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    int dev = 0, sms = 0, per_sm = 0;
+    if (!rc) rc = cuda_status(cudaGetDevice(&dev));
+    if (!rc) rc = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (!rc) rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+    if (!rc && per_sm < 1) rc = TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidConfiguration;
+    if (!rc) {
+        const int64_t cap = (int64_t)sms * per_sm;
+        const unsigned grid = (unsigned)(tb < cap ? tb : cap);
+        const int ni = (int)n;
+        const int64_t limit = int64_t(1) << 25;  // flag polls (64 ns apart at least) before giving up
+        void *args[] = {(void *)&L, (void *)&lda, (void *)&m, (void *)&ni, (void *)&B, (void *)&ldb,
+                        (void *)&W, (void *)&alpha, (void *)&flags, (void *)&status, (void *)&limit};
+        rc = cuda_status(cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(256), args, smem, st));
+    }
+    if (inv_ms) {
+        cudaEventRecord(e[2], st);
+        cudaEventSynchronize(e[2]);
+        cudaEventElapsedTime(inv_ms, e[0], e[1]);
+        cudaEventElapsedTime(solve_ms, e[1], e[2]);
+        for (auto &x : e) cudaEventDestroy(x);
+    }
+    return rc;
+}
+
 struct PhaseTimer {
     bool on = false;
     cudaStream_t st = nullptr;
@@ -187,6 +249,12 @@ struct PhaseTimer {
     }
 };
 
+template <typename T> constexpr int elem_code();
+template <> constexpr int elem_code<float>() { return 0; }
+template <> constexpr int elem_code<double>() { return 1; }
+template <> constexpr int elem_code<float2>() { return 2; }
+template <> constexpr int elem_code<double2>() { return 3; }
+
 template <typename T>
 int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     const int64_t m = a.m, n = a.n, nb = a.nb;
@@ -202,6 +270,16 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     void *tc_panels = nullptr;
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value)
         tc_panels = reinterpret_cast<char *>(Pw) + round256(nb * ldx * (int64_t)sizeof(T));
+
+    if (!a.tri_rhs && few_rhs_usable<T>(m, n, L, a.lda, blocked_workspace_bytes(elem_code<T>(), m, n, nb))) {
+        // a handful of columns: the persistent few-RHS kernel (profile: the
+        // inversion in ms[0], the solve in ms[2])
+        if (a.ms) a.ms[1] = 0.f;
+        T alpha0;
+        memcpy(&alpha0, a.alpha, sizeof(T));
+        return few_rhs_solve<T>(L, a.lda, m, n, B, a.ldb, alpha0, a.ws, st, a.ms ? &a.ms[0] : nullptr,
+                                a.ms ? &a.ms[2] : nullptr);
+    }
 
     PhaseTimer timer;
     int rc = TRSM_SUCCESS;
