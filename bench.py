@@ -684,6 +684,58 @@ def medium_bench(args):
             torch.cuda.empty_cache()
 
 
+def few_rhs_bench(args):
+    """One JSON line per (type, m, n) for few right-hand sides, n in
+    --few-ns: one system of order m (column-major, L strictly lower
+    U(-1,1)/m, diagonal 1 + U(0,1), B U(-1,1), alpha = 1; generated on the
+    device: timing only) through trsm_llnn_ex with the table's block size;
+    CUDA events after a warm-up solve, B restored before every run; GB/s
+    counts the algorithmic bytes (L's lower triangle once, B read, X written),
+    beside the phase split of trsm_llnn_profile."""
+    import torch
+
+    import triangular_solve_gb300 as tg
+    from triangular_solve_gb300 import build as tgb
+    tgb.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    for d in args.sweep_dtypes.split(","):
+        t = getattr(torch, TORCH_NAME[d])
+        real_t = torch.float32 if d in ("f32", "c64") else torch.float64
+        for mm in [int(x) for x in args.sweep_ms.split(",")]:
+            g = torch.Generator(device=dev).manual_seed(0)
+            lv = (torch.rand((mm, mm), generator=g, device=dev, dtype=real_t) * 2 - 1) / mm
+            lv.diagonal().copy_(1 + torch.rand(mm, generator=g, device=dev, dtype=real_t))
+            a = lv.to(t).t().contiguous().t()
+            del lv
+            for nn in [int(x) for x in args.few_ns.split(",")]:
+                b0 = (torch.rand((mm, nn), generator=g, device=dev, dtype=real_t) * 2 - 1).to(t).t().contiguous().t()
+                b = b0.clone()
+                wsb = tg.trsm_llnn_workspace_bytes(d, mm, nn, 0)
+                wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+                tg.trsm_llnn_ex(d, mm, nn, 1.0, a, mm, b, mm, 0, wsp, wsb, stream)
+                times = []
+                for _ in range(max(args.sweep_reps, 1)):
+                    b.copy_(b0)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    tg.trsm_llnn_ex(d, mm, nn, 1.0, a, mm, b, mm, 0, wsp, wsb, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                b.copy_(b0)
+                ph = tg.trsm_llnn_profile(d, mm, nn, 1.0, a, mm, b, mm, 0, wsp, wsb, stream)
+                ms = statistics.mean(times)
+                print(json.dumps({"op": "few_rhs", "dtype": d, "m": mm, "n": nn, "ms": round(ms, 4),
+                                  "gbs": round(ti.algorithmic_bytes(d, mm, nn) / (ms * 1e-3) / 1e9, 1),
+                                  "gflops": round(ti.flops(d, mm, nn) / (ms * 1e-3) / 1e9, 1),
+                                  "phases_ms": [round(x, 4) for x in ph],
+                                  "device_status": tg.trsm_device_status()}), flush=True)
+                del b0, b, wsp
+            del a
+            torch.cuda.empty_cache()
+
+
 def trtri_bench(args):
     """One JSON line per (type, m): the triangular inverse L^-1 through
     trsm_trtri_lower (set to I, then the L X = I solve), CUDA events on the
@@ -880,6 +932,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--variants", action="store_true",
                     help="time every TRSM variant (trsm_general) at m = n = --sweep-ms per --sweep-dtypes")
+    ap.add_argument("--few-rhs", action="store_true",
+                    help="time few right-hand sides (--few-ns) at m = --sweep-ms per --sweep-dtypes")
+    ap.add_argument("--few-ns", default="1,8")
     ap.add_argument("--medium", action="store_true",
                     help="time strided batches (--batch) of m = n = --sweep-ms systems per --sweep-dtypes")
     ap.add_argument("--batch", type=int, default=1024)
@@ -901,6 +956,9 @@ def main():
         return
     if args.medium:
         medium_bench(args)
+        return
+    if args.few_rhs:
+        few_rhs_bench(args)
         return
     if args.variants:
         variants_bench(args)

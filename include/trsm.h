@@ -73,7 +73,10 @@ typedef enum { TRSM_NONUNIT = 0, TRSM_UNIT = 1 } trsm_diag_t;
  * runs the blocked path of "Hierarchical Shared Memory-Aware Optimization for
  * TRSM on GPU Platforms" (diagonal-block inversion, then per block row an
  * apply X_t = D_t^{-1} R_t and a trailing GEMM update), with the block size
- * NB taken from the library's compile-time table.  The blocked path needs a
+ * NB taken from the library's compile-time table; with n <= 8 right-hand
+ * sides, m > 512 and 16-byte aligned columns of A, the same algorithm runs
+ * as one cooperative persistent launch over 128-row block rows (also through
+ * trsm_llnn_ex when its nb is 0 or 128).  The blocked path needs a
  * device workspace of trsm_llnn_workspace_bytes(dtype, m, n, 0) bytes; this
  * entry point allocates it with cudaMallocAsync on `stream` and frees it with
  * cudaFreeAsync on the same stream.  Use trsm_llnn_ex to pass your own.
@@ -91,8 +94,14 @@ int trsm_llnn(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
  * llama.cpp PR 17457 (its 4-D tensors flattened to one batch index).
  *
  * m <= 64: one launch of the small-regime kernel over the whole batch.
- * m > 64: the blocked path runs system by system on `stream` (correct, not
- * tuned for throughput), allocating its workspace as trsm_llnn does.
+ * m = 128 (column-major, 16-byte aligned columns): one launch of the
+ * chunked on-chip kernel over the whole batch.  Other m <= 2048: the blocked
+ * path over the whole batch in one sequence of launches (the system index in
+ * every kernel's grid; one inversion for all systems when strideA == 0),
+ * chunked to at most 65535 systems and 1 GiB of workspace per chunk.
+ * Larger m: the blocked path system by system.  The workspace of the blocked
+ * paths is allocated with cudaMallocAsync on `stream` and freed on it, as in
+ * trsm_llnn.
  *
  * Arguments: 1 dtype, 2 layout, 3 m, 4 n, 5 alpha, 6 A, 7 lda, 8 strideA,
  * 9 B, 10 ldb, 11 strideB, 12 batch, 13 stream.
@@ -173,7 +182,9 @@ int trsm_llnn_ex(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
  * X_t = D_t^{-1} R_t, ms[2] the trailing GEMM updates, in milliseconds (the
  * split reported in "Hierarchical Shared Memory-Aware Optimization for TRSM
  * on GPU Platforms", Table 3).  For m <= 64 the whole solve is reported in
- * ms[1] and the other two are 0.  ms must point to 3 host floats.
+ * ms[1] and the other two are 0; for the few-right-hand-sides launch the
+ * applies and updates run together and are reported in ms[2] (ms[1] = 0).
+ * ms must point to 3 host floats.
  *
  * Arguments: 1..12 as trsm_llnn_ex, 13 ms.
  */
@@ -215,10 +226,12 @@ int trsm_general(trsm_dtype_t dtype, trsm_side_t side, trsm_uplo_t uplo, trsm_op
  * of A is never read), into Ainv (m x m, column-major, ldinv >= max(1,m)),
  * whose strictly upper part is set to zero.  Computed as the solve
  * L Ainv = I on `stream` (Ainv is set to the identity, then solved in place
- * by the path trsm_llnn takes, with the same workspace allocation), so it
- * costs the m^3 flops of that solve rather than TRTRI's m^3/3; the
- * diagonal-block inverses of "Hierarchical Shared Memory-Aware Optimization
- * for TRSM on GPU Platforms" are its first phase.  Ainv must not overlap A.
+ * by the path trsm_llnn takes, with the same workspace allocation).  Every
+ * product of that solve is restricted to the columns of the identity that
+ * can be nonzero at its step, so the inverse costs TRTRI's m^3/3 flops
+ * rather than the m^3 of a general solve; the diagonal-block inverses of
+ * "Hierarchical Shared Memory-Aware Optimization for TRSM on GPU Platforms"
+ * are its first phase.  Ainv must not overlap A.
  * A zero on the diagonal gives IEEE infinities / NaN, no status.
  *
  * Arguments: 1 dtype, 2 m, 3 A, 4 lda, 5 Ainv, 6 ldinv, 7 stream.

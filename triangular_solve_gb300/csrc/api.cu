@@ -243,6 +243,7 @@ int solve_dispatch(int dtype, int layout, int64_t m, int64_t n, const void *alph
     }
 
     const int eb = elem_bytes(dtype);
+    const bool nb_from_table = nb == 0;
     if (nb == 0) nb = nearest_nb(dtype, m);
     if (batch > 1 && m <= kBatchedMaxM)
         return solve_batched(dtype, layout, m, n, s.alpha, A, lda, sA, B, ldb, sB, batch, nb, ws, ws_bytes,
@@ -268,6 +269,7 @@ int solve_dispatch(int dtype, int layout, int64_t m, int64_t n, const void *alph
         ba.ws = mem;
         ba.ms = ms;
         ba.tri_rhs = tri_rhs && batch == 1 && layout == TRSM_COL_MAJOR;
+        ba.nb_from_table = nb_from_table;
         memcpy(ba.alpha, s.alpha, sizeof(ba.alpha));
         const char *Ab = static_cast<const char *>(A) + b * sA * eb;
         char *Bb = static_cast<char *>(B) + b * sB * eb;

@@ -271,7 +271,8 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value)
         tc_panels = reinterpret_cast<char *>(Pw) + round256(nb * ldx * (int64_t)sizeof(T));
 
-    if (!a.tri_rhs && few_rhs_usable<T>(m, n, L, a.lda, blocked_workspace_bytes(elem_code<T>(), m, n, nb))) {
+    if (!a.tri_rhs && (a.nb_from_table || nb == kFewNB) &&
+        few_rhs_usable<T>(m, n, L, a.lda, blocked_workspace_bytes(elem_code<T>(), m, n, nb))) {
         // a handful of columns: the persistent few-RHS kernel (profile: the
         // inversion in ms[0], the solve in ms[2])
         if (a.ms) a.ms[1] = 0.f;
@@ -303,20 +304,20 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
 
     const int64_t tb = (m + nb - 1) / nb;
     if constexpr (std::is_same<T, float>::value) {
-        if (tc_panels && !a.tri_rhs && tc_fused_usable(m, n, nb)) {
+        if (tc_panels && tc_fused_usable(m, n, nb)) {
             // look-ahead form (tc_gemm.cu): every launch but the last is an
             // update with the previous block's apply folded in (phase 2);
             // the last holds the two remaining applies (phase 1)
             timer.begin();
             TcSide *side = nullptr;
             rc = tc_side_acquire(st, &side);
-            if (!rc) rc = tc_fused_prepare_side(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, side);
+            if (!rc) rc = tc_fused_prepare_side(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, side, a.tri_rhs);
             for (int64_t t = 0; !rc && t + 1 < tb; ++t)
-                rc = tc_fused_step_side(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, side);
+                rc = tc_fused_step_side(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, side, a.tri_rhs);
             tc_side_release(side);
             if (rc || (rc = timer.end(2))) return rc;
             timer.begin();
-            rc = tc_fused_step(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            rc = tc_fused_step(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, a.tri_rhs);
             if (rc || (rc = timer.end(1))) return rc;
             if (a.ms)
                 for (int q = 0; q < 3; ++q) a.ms[q] = timer.acc[q];
@@ -324,15 +325,15 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
         }
     }
     if constexpr (std::is_same<T, float2>::value) {
-        if (tc_panels && !a.tri_rhs && tc_fused_usable_c64(m, n, nb)) {
+        if (tc_panels && tc_fused_usable_c64(m, n, nb)) {
             // the look-ahead form in real form (tc_gemm.cu), phases as for f32
             timer.begin();
-            rc = tc_fused_prepare_c64(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st);
+            rc = tc_fused_prepare_c64(m, n, nb, L, a.lda, W, B, a.ldb, tc_panels, st, a.tri_rhs);
             for (int64_t t = 0; !rc && t + 1 < tb; ++t)
-                rc = tc_fused_step_c64(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+                rc = tc_fused_step_c64(t, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, a.tri_rhs);
             if (rc || (rc = timer.end(2))) return rc;
             timer.begin();
-            rc = tc_fused_step_c64(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st);
+            rc = tc_fused_step_c64(tb - 1, m, n, nb, L, a.lda, W, B, a.ldb, alpha, tc_panels, st, a.tri_rhs);
             if (rc || (rc = timer.end(1))) return rc;
             if (a.ms)
                 for (int q = 0; q < 3; ++q) a.ms[q] = timer.acc[q];

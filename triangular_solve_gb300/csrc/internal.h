@@ -60,6 +60,9 @@ struct BlockedArgs {
     // B holds the identity (alpha = 1): block row t's solve and update touch
     // only its first (t+1) nb columns (the triangular inverse)
     bool tri_rhs = false;
+    // nb is the table's choice (the caller passed 0), so a path with its own
+    // block size (few right-hand sides: 128) may take over
+    bool nb_from_table = true;
 };
 
 // Bytes of workspace the blocked path needs: the inverted diagonal blocks
@@ -107,16 +110,16 @@ int tc_apply_f32(int64_t mb, int64_t N, const float *Wt, int64_t nb, float *Bt, 
 bool tc_fused_usable(int64_t m, int64_t n, int64_t nb);
 size_t tc_fused_bytes(int64_t m, int64_t n, int64_t nb);
 int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
-                     int64_t ldb, void *panels, cudaStream_t st);
+                     int64_t ldb, void *panels, cudaStream_t st, bool tri = false);
 int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st);
+                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, bool tri = false);
 // The same for c64, in real form with interleaved K (tc_gemm.cu).
 bool tc_fused_usable_c64(int64_t m, int64_t n, int64_t nb);
 size_t tc_fused_bytes_c64(int64_t m, int64_t n, int64_t nb);
 int tc_fused_prepare_c64(int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
-                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st);
+                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st, bool tri = false);
 int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
-                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st);
+                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st, bool tri = false);
 // Tiled TMA tensor map of an f32 tensor (see tc_gemm.cu).
 int encode_f32_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
                    const uint32_t *box, bool swizzle128);

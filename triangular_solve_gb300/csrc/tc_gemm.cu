@@ -435,6 +435,10 @@ struct TcFused {
 
 int64_t round_rows(int64_t r) { return (r + 255) / 256 * 256; }
 
+// Columns a product must cover: all n, or with a lower-triangular identity
+// right-hand side (tri) only the first `upto` of them.
+int64_t tri_cols(bool tri, int64_t n, int64_t upto) { return (tri && upto < n) ? upto : n; }
+
 TcFused tc_fused_layout(void *panels, int64_t m, int64_t n, int64_t nb) {
     TcFused f;
     f.ra = round_rows(m);
@@ -596,9 +600,10 @@ void tc_side_release(TcSide *side) {
 // This launch counts as launch -1 for the side stream (it reads block 0's
 // operand buffers, which block 2's overwrite).
 int tc_fused_prepare_side(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                          const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side) {
+                          const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side, bool tri) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
-    int rc = split_rows(B, ldb, n, nb, f.xs_hi[0], f.xs_lo[0], nb, st);  // columns of R_0
+    // columns of R_0 (tri: the first two blocks, all update 0 reads)
+    int rc = split_rows(B, ldb, tri_cols(tri, n, 2 * nb), nb, f.xs_hi[0], f.xs_lo[0], nb, st);
     if (!rc) rc = tc_w_splits(f, 0, m, nb, L, lda, W, st);
     if (!rc && 2 * nb < m) rc = tc_w_splits(f, 1, m, nb, L, lda, W, st);
     if (rc) return rc;
@@ -615,7 +620,7 @@ int tc_fused_prepare_side(int64_t m, int64_t n, int64_t nb, const float *L, int6
 // launch t-1 is done (their buffers were last read by it), and launch t
 // waits for block t+1's.
 int tc_fused_step_side(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                       float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, TcSide *side) {
+                       float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, TcSide *side, bool tri) {
     const TcFused f = tc_fused_layout(panels, m, n, nb);
     const int64_t tb = (m + nb - 1) / nb, r0 = t * nb;
     int rc;
@@ -629,7 +634,7 @@ int tc_fused_step_side(int64_t t, int64_t m, int64_t n, int64_t nb, const float 
     TcLaunch P;
     int np = 0;
     if (t + 1 < tb) {
-        TcArgs g = tc_args(m - r0 - nb, n, nb, B + r0 + nb, ldb);
+        TcArgs g = tc_args(m - r0 - nb, tri_cols(tri, n, (t + 2) * nb), nb, B + r0 + nb, ldb);
         g.beta = t == 0 ? alpha : 1.f;
         g.gamma = t == 0 ? -alpha : -1.f;
         g.xhi = f.xs_hi[(t + 1) % 3];
@@ -645,26 +650,35 @@ int tc_fused_step_side(int64_t t, int64_t m, int64_t n, int64_t nb, const float 
                 return cuda_status(e);
             if ((rc = tc_w_problem(P.p[np++], f, t + 1, m, nb))) return rc;
         }
-    } else if ((rc = tc_x_problem(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : 1.f, f.d1_hi[0],
-                                  f.d1_lo[0], st))) {
+    } else if ((rc = tc_x_problem(P.p[np++], f, t, m, tri_cols(tri, n, (t + 1) * nb), nb, W, B, ldb,
+                                  t == 0 ? alpha : 1.f, f.d1_hi[0], f.d1_lo[0], st))) {
         return rc;
     }
-    if (t >= 1 &&
-        (rc = tc_x_problem(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : 1.f, f.d0_hi, f.d0_lo, st)))
+    if (t >= 1 && (rc = tc_x_problem(P.p[np++], f, t - 1, m, tri_cols(tri, n, t * nb), nb, W, B, ldb,
+                                     t == 1 ? alpha : 1.f, f.d0_hi, f.d0_lo, st)))
         return rc;
     if ((rc = tc_launch(P, np, st))) return rc;
     if (side && (e = cudaEventRecord(side->launched[t & 1], st)) != cudaSuccess) return cuda_status(e);
+    if (tri && (t + 2) * nb < n) {
+        // update t+1 reads R_{t+1} over its first (t+3) nb columns; the
+        // epilogue above split the first (t+2) nb, the next block of them is
+        // zero (those columns of the identity start below block t+1)
+        const int64_t j0 = (t + 2) * nb, rows = (n - j0 < nb) ? n - j0 : nb;
+        const size_t off = (size_t)(j0 * nb), bytes = (size_t)(rows * nb) * sizeof(float);
+        if ((e = cudaMemsetAsync(f.xs_hi[(t + 1) % 3] + off, 0, bytes, st)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaMemsetAsync(f.xs_lo[(t + 1) % 3] + off, 0, bytes, st)) != cudaSuccess) return cuda_status(e);
+    }
     return TRSM_SUCCESS;
 }
 
 int tc_fused_prepare(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W, const float *B,
-                     int64_t ldb, void *panels, cudaStream_t st) {
-    return tc_fused_prepare_side(m, n, nb, L, lda, W, B, ldb, panels, st, nullptr);
+                     int64_t ldb, void *panels, cudaStream_t st, bool tri) {
+    return tc_fused_prepare_side(m, n, nb, L, lda, W, B, ldb, panels, st, nullptr, tri);
 }
 
 int tc_fused_step(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st) {
-    return tc_fused_step_side(t, m, n, nb, L, lda, W, B, ldb, alpha, panels, st, nullptr);
+                  float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, bool tri) {
+    return tc_fused_step_side(t, m, n, nb, L, lda, W, B, ldb, alpha, panels, st, nullptr, tri);
 }
 
 // ---------------------------------------------------------------------------
@@ -771,10 +785,11 @@ size_t tc_fused_bytes_c64(int64_t m, int64_t n, int64_t nb) {
 }
 
 int tc_fused_prepare_c64(int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
-                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st) {
+                         const float2 *B, int64_t ldb, void *panels, cudaStream_t st, bool tri) {
     const TcFusedC64 f = tc_fused_layout_c64(panels, m, n, nb);
-    split_c64_xi_kernel<<<dim3((unsigned)((nb + 127) / 128), (unsigned)(n < 65535 ? n : 65535)), 128, 0, st>>>(
-        B, ldb, nb, n, f.xs_hi[0], f.xs_lo[0], 2 * nb);  // R_0, interleaved X'
+    const int64_t n0 = tri_cols(tri, n, 2 * nb);  // tri: the columns update 0 reads
+    split_c64_xi_kernel<<<dim3((unsigned)((nb + 127) / 128), (unsigned)(n0 < 65535 ? n0 : 65535)), 128, 0, st>>>(
+        B, ldb, nb, n0, f.xs_hi[0], f.xs_lo[0], 2 * nb);  // R_0, interleaved X'
     int rc = launch_status();
     if (rc) return rc;
     TcLaunch P;
@@ -783,7 +798,7 @@ int tc_fused_prepare_c64(int64_t m, int64_t n, int64_t nb, const float2 *L, int6
 }
 
 int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 *L, int64_t lda, const float2 *W,
-                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st) {
+                      float2 *B, int64_t ldb, float2 alpha, void *panels, cudaStream_t st, bool tri) {
     const TcFusedC64 f = tc_fused_layout_c64(panels, m, n, nb);
     const int64_t tb = (m + nb - 1) / nb, r0 = t * nb;
     const float2 one = make_float2(1.f, 0.f);
@@ -791,7 +806,8 @@ int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 
     TcLaunch P;
     int np = 0;
     if (t + 1 < tb) {
-        TcArgs g = tc_args(m - r0 - nb, 2 * n, 2 * nb, reinterpret_cast<float *>(B + r0 + nb), 2 * ldb);
+        TcArgs g = tc_args(m - r0 - nb, 2 * tri_cols(tri, n, (t + 2) * nb), 2 * nb,
+                           reinterpret_cast<float *>(B + r0 + nb), 2 * ldb);
         const float2 beta = t == 0 ? alpha : one;
         g.beta = beta.x;
         g.beta_im = beta.y;
@@ -807,14 +823,24 @@ int tc_fused_step_c64(int64_t t, int64_t m, int64_t n, int64_t nb, const float2 
                              2 * f.rx, 2 * nb, g)))
             return rc;
         if (r0 + 2 * nb < m && (rc = tc_w_problem_c64(P.p[np++], f, t + 1, m, nb, L, lda, W, st))) return rc;
-    } else if ((rc = tc_x_problem_c64(P.p[np++], f, t, m, n, nb, W, B, ldb, t == 0 ? alpha : one, f.d1_hi,
-                                      f.d1_lo, st))) {
+    } else if ((rc = tc_x_problem_c64(P.p[np++], f, t, m, tri_cols(tri, n, (t + 1) * nb), nb, W, B, ldb,
+                                      t == 0 ? alpha : one, f.d1_hi, f.d1_lo, st))) {
         return rc;
     }
-    if (t >= 1 && (rc = tc_x_problem_c64(P.p[np++], f, t - 1, m, n, nb, W, B, ldb, t == 1 ? alpha : one, f.d0_hi,
-                                         f.d0_lo, st)))
+    if (t >= 1 && (rc = tc_x_problem_c64(P.p[np++], f, t - 1, m, tri_cols(tri, n, t * nb), nb, W, B, ldb,
+                                         t == 1 ? alpha : one, f.d0_hi, f.d0_lo, st)))
         return rc;
-    return tc_launch(P, np, st);
+    if ((rc = tc_launch(P, np, st))) return rc;
+    if (tri && (t + 2) * nb < n) {
+        // as for f32: the next block of R_{t+1}'s columns is zero (rows 2j,
+        // 2j+1 of the interleaved panel for column j)
+        const int64_t j0 = (t + 2) * nb, rows = (n - j0 < nb) ? n - j0 : nb;
+        const size_t off = (size_t)(2 * j0 * 2 * nb), bytes = (size_t)(2 * rows * 2 * nb) * sizeof(float);
+        cudaError_t e;
+        if ((e = cudaMemsetAsync(f.xs_hi[(t + 1) % 3] + off, 0, bytes, st)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaMemsetAsync(f.xs_lo[(t + 1) % 3] + off, 0, bytes, st)) != cudaSuccess) return cuda_status(e);
+    }
+    return TRSM_SUCCESS;
 }
 
 namespace {

@@ -26,9 +26,11 @@ struct TcSide {
 int tc_side_acquire(cudaStream_t st, TcSide **side);
 void tc_side_release(TcSide *side);
 // tc_fused_prepare / tc_fused_step with the side stream (nullptr: none)
+// tri: B is the identity (the triangular inverse); each product covers only
+// the columns that can be nonzero at its step.
 int tc_fused_prepare_side(int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                          const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side);
+                          const float *B, int64_t ldb, void *panels, cudaStream_t st, TcSide *side, bool tri);
 int tc_fused_step_side(int64_t t, int64_t m, int64_t n, int64_t nb, const float *L, int64_t lda, const float *W,
-                       float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, TcSide *side);
+                       float *B, int64_t ldb, float alpha, void *panels, cudaStream_t st, TcSide *side, bool tri);
 
 }  // namespace trsm
