@@ -192,7 +192,8 @@ static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, in
     if (!rc) rc = device_status_word(&status);
     if (inv_ms) cudaEventRecord(e[1], st);
     constexpr size_t smem = few_rhs_smem<T>();
-    auto kern = few_rhs_kernel<T>;
+    auto kern = n <= 1 ? few_rhs_kernel<T, 1> : n <= 2 ? few_rhs_kernel<T, 2> : n <= 4 ? few_rhs_kernel<T, 4>
+                                                                                       : few_rhs_kernel<T, 8>;
     if (!rc) rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     int dev = 0, sms = 0, per_sm = 0;
     if (!rc) rc = cuda_status(cudaGetDevice(&dev));

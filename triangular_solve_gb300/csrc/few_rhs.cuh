@@ -37,6 +37,11 @@ struct FewCfg {
         (size_t)ST * kChunk * sizeof(T) + 2 * (size_t)kFewNB * kFewMaxN * sizeof(T);
 };
 
+__device__ __forceinline__ float add2_(float a, float b) { return a + b; }
+__device__ __forceinline__ double add2_(double a, double b) { return a + b; }
+__device__ __forceinline__ float2 add2_(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ double2 add2_(double2 a, double2 b) { return make_double2(a.x + b.x, a.y + b.y); }
+
 __device__ __forceinline__ int ld_acquire_flag(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
@@ -49,7 +54,11 @@ __device__ __forceinline__ void st_release_flag(int *p, int v) {
 // 256 threads: thread (row, half) = (tid % 128, tid / 128); a chunk's KC
 // columns are split between the two halves, whose partial sums meet in
 // shared memory at the end of each block row.
-template <typename T>
+// NC: right-hand sides the registers and loops are sized for (n <= NC; the
+// launcher picks the smallest of 1, 2, 4, 8): a guarded loop over a fixed
+// eight would still issue the idle columns' FMAs, which on the FP64 pipe
+// cost as much as the real ones.
+template <typename T, int NC>
 __global__ void __launch_bounds__(256, 1)
     few_rhs_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int n, T *B, int64_t ldb,
                    const T *__restrict__ W, const T alpha, int *flags, int *status, const int64_t wait_limit) {
@@ -97,9 +106,9 @@ __global__ void __launch_bounds__(256, 1)
             if (c < nchunks) issue(c);
             cp_async_commit();
         }
-        T acc[kFewMaxN];
+        T acc[NC];
 #pragma unroll
-        for (int c = 0; c < kFewMaxN; ++c) acc[c] = zero_of<T>();
+        for (int c = 0; c < NC; ++c) acc[c] = zero_of<T>();
 
         for (int64_t c = 0; c < nchunks; ++c) {
             const int64_t s = c / KPT;
@@ -122,28 +131,31 @@ __global__ void __launch_bounds__(256, 1)
                         cp_async_wait_all();
                         return;
                     }
-                    for (int e = tid; e < NB * n; e += 256) {
-                        const int i = e / n, cc = e % n;
-                        xs[i * kFewMaxN + cc] = __ldcg(B + cc * ldb + s * NB + i);
+                    for (int e = tid; e < NB * NC; e += 256) {
+                        const int i = e / NC, cc = e % NC;
+                        xs[i * kFewMaxN + cc] = cc < n ? __ldcg(B + cc * ldb + s * NB + i) : zero_of<T>();
                     }
                 } else {
                     // every tile is in: r_t = alpha b_t - sum_s L_ts x_s
                     if (half == 1) {
 #pragma unroll
-                        for (int cc = 0; cc < kFewMaxN; ++cc)
+                        for (int cc = 0; cc < NC; ++cc)
                             if (cc < n) part[row * kFewMaxN + cc] = acc[cc];
                     }
                     __syncthreads();
                     if (half == 0) {
 #pragma unroll
-                        for (int cc = 0; cc < kFewMaxN; ++cc) {
+                        for (int cc = 0; cc < NC; ++cc) {
                             if (cc >= n) continue;
                             const T b = (r0 + row < m) ? B[cc * ldb + r0 + row] : zero_of<T>();
                             xs[row * kFewMaxN + cc] = sub_(sub_(mul(alpha, b), acc[cc]), part[row * kFewMaxN + cc]);
                         }
+#pragma unroll
+                        for (int cc = 0; cc < NC; ++cc)
+                            if (cc >= n) xs[row * kFewMaxN + cc] = zero_of<T>();
                     }
 #pragma unroll
-                    for (int cc = 0; cc < kFewMaxN; ++cc) acc[cc] = zero_of<T>();
+                    for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
                 }
             }
             cp_async_wait<ST - 2>();
@@ -152,27 +164,35 @@ __global__ void __launch_bounds__(256, 1)
             cp_async_commit();
             const T *ch = ring + (c % ST) * C::kChunk;
             const int k0 = (int)(c % KPT) * KC;
+            // two partial sums per column (even / odd j): independent FMA chains
+            T acc2[NC];
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) acc2[cc] = zero_of<T>();
 #pragma unroll 4
-            for (int jj = 0; jj < KC / 2; ++jj) {
+            for (int jj = 0; jj < KC / 2; jj += 2) {
                 const int j = half * (KC / 2) + jj;
-                const T a = ch[j * NB + row];
+                const T a0 = ch[j * NB + row], a1 = ch[(j + 1) * NB + row];
                 const T *xk = xs + (k0 + j) * kFewMaxN;
 #pragma unroll
-                for (int cc = 0; cc < kFewMaxN; ++cc)
-                    if (cc < n) acc[cc] = fma_(a, xk[cc], acc[cc]);
+                for (int cc = 0; cc < NC; ++cc) {
+                    acc[cc] = fma_(a0, xk[cc], acc[cc]);
+                    acc2[cc] = fma_(a1, xk[kFewMaxN + cc], acc2[cc]);
+                }
             }
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], acc2[cc]);
         }
         // x_t = W_t r_t: the halves meet, X goes over b_t, then the flag
         __syncthreads();
         if (half == 1) {
 #pragma unroll
-            for (int cc = 0; cc < kFewMaxN; ++cc)
+            for (int cc = 0; cc < NC; ++cc)
                 if (cc < n) part[row * kFewMaxN + cc] = acc[cc];
         }
         __syncthreads();
         if (half == 0 && r0 + row < m) {
 #pragma unroll
-            for (int cc = 0; cc < kFewMaxN; ++cc) {
+            for (int cc = 0; cc < NC; ++cc) {
                 if (cc >= n) continue;
                 const T p = part[row * kFewMaxN + cc];
                 B[cc * ldb + r0 + row] = fma_(one_of<T>(), p, acc[cc]);
