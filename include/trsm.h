@@ -155,7 +155,9 @@ int trsm_llnn_select_nb(trsm_dtype_t dtype, int64_t m, int64_t n);
  * block size nb (nb == 0: the table's choice; otherwise one of 128, 256,
  * 512).  0 when m <= 64.  Returns (size_t)-1 for invalid arguments.
  * The workspace holds the inverted diagonal blocks D_t^{-1} (m x NB) and one
- * NB x n panel of X.
+ * NB x n panel of X; with n <= 8 it is at least what the few-right-hand-side
+ * kernel keeps there (the inverted 128-row diagonal blocks and a copy of X,
+ * each rounded up to 256 bytes).
  */
 size_t trsm_llnn_workspace_bytes(trsm_dtype_t dtype, int64_t m, int64_t n, int64_t nb);
 

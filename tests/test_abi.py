@@ -62,6 +62,23 @@ def test_workspace_bytes(lib):
         tg.trsm_llnn_workspace_bytes("f32", 1000, 70, 100)
 
 
+def test_workspace_bytes_few_rhs(lib):
+    """n <= 8: at least the few-right-hand-side kernel's data -- the inverted
+    128-row diagonal blocks and the published copy of X (ceil(m/128) block
+    rows of 128 x n), each rounded up to 256 bytes."""
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    for d, e in (("f64", 8), ("c128", 16)):
+        for m, n in ((4096, 1), (16384, 8), (1000, 3)):
+            tb = (m + 127) // 128
+            few = r(tb * 128 * 128 * e) + r(tb * n * 128 * e)
+            for nb in (128, 256, 512):
+                tbn = (m + nb - 1) // nb
+                blocked = r(tbn * nb * nb * e) + 2 * r(nb * ((n + 3) // 4 * 4) * e)
+                assert tg.trsm_llnn_workspace_bytes(d, m, n, nb) == max(few, blocked)
+    # from nine columns on only the blocked path's own terms
+    assert tg.trsm_llnn_workspace_bytes("f64", 4096, 9, 128) == r(32 * 128 * 128 * 8) + 2 * r(128 * 12 * 8)
+
+
 def test_workspace_bytes_lookahead_form(lib):
     """f32 with n >= 256 and a last block of at least 16 rows takes the
     look-ahead form; its panels (rows padded to 256): the scaled L panel and

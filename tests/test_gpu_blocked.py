@@ -178,15 +178,26 @@ def test_narrow_path_large(env, dtype):
 @pytest.mark.parametrize("m,n", [(513, 1), (640, 8), (1000, 2), (2049, 5), (4096, 3)])
 def test_few_rhs_persistent_path(env, dtype, m, n):
     """n <= 8 with 16-byte aligned columns of L: the persistent few-right-hand-
-    side kernel (one CTA per 128-row block row, flags between them), ragged
-    last block rows, complex alpha, padded leading dimensions; the device
-    status word stays clear."""
-    pad = {"f32": 4, "f64": 2, "c64": 2, "c128": 1}[dtype]  # keeps every column 16-byte aligned
+    side kernel (one CTA per 128-row block row, each publishing its x_t to
+    the CTAs below), ragged last block rows, complex alpha, padded leading
+    dimensions; the device status word stays clear, and the phase times show
+    that this kernel ran (no separate applies)."""
+    torch, tg = env["torch"], env["tg"]
+    per16 = {"f32": 4, "f64": 2, "c64": 2, "c128": 1}[dtype]  # elements in 16 bytes
+    lda = (m + per16 - 1) // per16 * per16 + per16           # padded, every column 16-byte aligned
     L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=m + 31 * n)
     alpha = (0.5 + 1.25j) if ti.IS_COMPLEX[dtype] else -1.25
-    xg, xr = _ex_solve(env, dtype, L, B, alpha, 0, lda=m + pad, ldb=m + 3)
-    assert env["tg"].trsm_device_status() == 0
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, 0, lda=lda, ldb=m + 3)
+    assert tg.trsm_device_status() == 0
     assert_parity(dtype, xg, xr, f"few-rhs {dtype} m={m} n={n}")
+
+    a, b, geo = storage_pair(L, B, lda=lda, ldb=m + 3)
+    ws_bytes = tg.trsm_llnn_workspace_bytes(dtype, m, n, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ms = tg.trsm_llnn_profile(dtype, m, n, alpha, tA, geo["lda"], tB, geo["ldb"], 0, ws, ws_bytes)
+    assert ms[1] == 0.0 and ms[2] > 0.0, f"few-rhs {dtype} m={m} n={n}: phases {ms}"
+    assert_parity(dtype, logical(tB.cpu().numpy(), geo), xr, f"few-rhs profiled {dtype} m={m} n={n}")
 
 
 @pytest.mark.parametrize("m,n,nb,ld_pad", [

@@ -159,35 +159,48 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
 
 // The few-right-hand-sides path (few_rhs.cuh): n <= kFewMaxN columns of a
 // column-major system of order m > kFewMinM, 16-byte aligned L columns, and
-// its data -- the inverted 128-row diagonal blocks, then one flag per block
-// row -- within the blocked path's workspace of ws_bytes.
+// its data (few_rhs_bytes, which blocked_workspace_bytes covers) within the
+// workspace of ws_bytes.
 constexpr int64_t kFewMinM = 512;
-inline size_t few_rhs_bytes(int64_t m, int elem_bytes) {
-    const int64_t tb = (m + kFewNB - 1) / kFewNB;
-    return (size_t)(round256(tb * kFewNB * kFewNB * elem_bytes) + round256(tb * 4));
-}
 
 template <typename T>
 static bool few_rhs_usable(int64_t m, int64_t n, const T *L, int64_t lda, size_t ws_bytes) {
     return n >= 1 && n <= kFewMaxN && m > kFewMinM && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) &&
-           (lda * (int64_t)sizeof(T)) % 16 == 0 && few_rhs_bytes(m, (int)sizeof(T)) <= ws_bytes;
+           (lda * (int64_t)sizeof(T)) % 16 == 0 && few_rhs_bytes((int)sizeof(T), m, n) <= ws_bytes;
 }
 
-// The inversion of the 128-row diagonal blocks, then the persistent kernel
-// (a cooperative launch: its CTAs wait on one another's flags, so all of them
-// must be resident at once).
+// The inversion of the diagonal blocks (few_nb<T>() rows), then the
+// persistent kernel (a cooperative launch: its CTAs wait on one another's
+// published results, so all of them must be resident at once).  L and the inverted
+// blocks are read by TMA tensor copies: float views, a column's block of
+// rows as boxes of at most 256 floats.
 template <typename T>
 static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, int64_t ldb, T alpha, void *ws,
                          cudaStream_t st, float *inv_ms, float *solve_ms) {
-    const int64_t tb = (m + kFewNB - 1) / kFewNB;
+    using Cfg = FewCfg<T>;
+    constexpr int64_t NB = Cfg::NB;
+    const int64_t tb = (m + NB - 1) / NB;
     T *W = static_cast<T *>(ws);
-    int *flags = reinterpret_cast<int *>(static_cast<char *>(ws) + round256(tb * kFewNB * kFewNB * (int64_t)sizeof(T)));
+    T *xpub = reinterpret_cast<T *>(static_cast<char *>(ws) + round256(tb * NB * NB * (int64_t)sizeof(T)));
+    CUtensorMap mapL, mapW;
+    {
+        const uint64_t dl[3] = {(uint64_t)(m * Cfg::Q), (uint64_t)m, 1};
+        const uint64_t sl[2] = {(uint64_t)(lda * (int64_t)sizeof(T)), (uint64_t)(lda * (int64_t)sizeof(T) * m)};
+        const uint32_t box[3] = {(uint32_t)(Cfg::BR * Cfg::Q), (uint32_t)Cfg::KC, 1};
+        int rc = encode_f32_map(&mapL, L, 3, dl, sl, box, false);
+        if (rc) return rc;
+        const uint64_t dw[3] = {(uint64_t)(NB * Cfg::Q), (uint64_t)(tb * NB), 1};
+        const uint64_t sw[2] = {(uint64_t)(NB * (int64_t)sizeof(T)), (uint64_t)(NB * (int64_t)sizeof(T) * tb * NB)};
+        rc = encode_f32_map(&mapW, W, 3, dw, sw, box, false);
+        if (rc) return rc;
+    }
     cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
     if (inv_ms)
         for (auto &x : e) cudaEventCreate(&x);
     if (inv_ms) cudaEventRecord(e[0], st);
-    int rc = invert_diagonal_blocks<T, kFewNB / 8>(L, lda, m, kFewNB, W, st);
-    if (!rc) rc = cuda_status(cudaMemsetAsync(flags, 0, (size_t)tb * sizeof(int), st));
+    int rc = invert_diagonal_blocks<T, (int)NB / 8>(L, lda, m, (int)NB, W, st);
+    // every word of the published copy unset (all ones) until written
+    if (!rc) rc = cuda_status(cudaMemsetAsync(xpub, 0xff, (size_t)(tb * n * NB) * sizeof(T), st));
     int *status = nullptr;
     if (!rc) rc = device_status_word(&status);
     if (inv_ms) cudaEventRecord(e[1], st);
@@ -198,16 +211,16 @@ static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, in
     int dev = 0, sms = 0, per_sm = 0;
     if (!rc) rc = cuda_status(cudaGetDevice(&dev));
     if (!rc) rc = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    if (!rc) rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+    if (!rc) rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 320, smem));
     if (!rc && per_sm < 1) rc = TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidConfiguration;
     if (!rc) {
         const int64_t cap = (int64_t)sms * per_sm;
         const unsigned grid = (unsigned)(tb < cap ? tb : cap);
         const int ni = (int)n;
-        const int64_t limit = int64_t(1) << 25;  // flag polls (64 ns apart at least) before giving up
-        void *args[] = {(void *)&L, (void *)&lda, (void *)&m, (void *)&ni, (void *)&B, (void *)&ldb,
-                        (void *)&W, (void *)&alpha, (void *)&flags, (void *)&status, (void *)&limit};
-        rc = cuda_status(cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(256), args, smem, st));
+        const int64_t limit = int64_t(1) << 22;  // polls of a published block row (each a round trip to L2)
+        void *args[] = {(void *)&mapL, (void *)&mapW, (void *)&m, (void *)&ni, (void *)&B, (void *)&ldb,
+                        (void *)&alpha, (void *)&xpub, (void *)&status, (void *)&limit};
+        rc = cuda_status(cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(320), args, smem, st));
     }
     if (inv_ms) {
         cudaEventRecord(e[2], st);
@@ -272,7 +285,7 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
     if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value)
         tc_panels = reinterpret_cast<char *>(Pw) + round256(nb * ldx * (int64_t)sizeof(T));
 
-    if (!a.tri_rhs && (a.nb_from_table || nb == kFewNB) &&
+    if (!a.tri_rhs && (a.nb_from_table || nb == few_nb<T>()) &&
         few_rhs_usable<T>(m, n, L, a.lda, blocked_workspace_bytes(elem_code<T>(), m, n, nb))) {
         // a handful of columns: the persistent few-RHS kernel (profile: the
         // inversion in ms[0], the solve in ms[2])

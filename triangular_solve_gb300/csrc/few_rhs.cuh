@@ -9,32 +9,58 @@
 //     x_t = W_t (alpha b_t - sum_{s<t} L_ts x_s)
 // -- but runs all block rows in one cooperatively launched persistent
 // kernel.  The CTA that owns block row t streams its tiles L_ts (s < t) and
-// then W_t through a ring of cp.async stages, independently of the solve, so
-// every tile is on chip before it is needed; it folds tile s in as soon as
-// the owner of block row s has published x_s (a flag per block row, waits
-// bounded), and publishes x_t in turn.  The reduction sum_{s<t} L_ts x_s is
-// therefore spread over the owners of the block rows below, in parallel,
-// and only one 128 x 128 product and the application of W_t per block row
-// lie on the dependency chain.
+// then W_t on chip, independently of the solve, folds tile s in as soon as
+// the owner of block row s has published x_s, and publishes x_t in turn.
+// The reduction sum_{s<t} L_ts x_s is spread over the owners of the block
+// rows below, in parallel; only one 128 x 128 product and the application of
+// W_t per block row lie on the dependency chain.
+//
+// Roles inside a CTA (warp specialised, no CTA-wide barrier after set-up):
+//   warp 0    issues the TMA tensor copies of the tiles, 128 rows x KC
+//             columns at a time, into a ring of mbarrier-tracked stages;
+//   warp 1    polls each block row's published x_s and stages it in a small
+//             ring of slots, a few tiles ahead of the consumers;
+//   warps 2-9 consume: thread (row, half) accumulates its row of L_ts x_s
+//             over half of each chunk's columns; the two halves meet in
+//             shared memory once per block row.
+// Every wait is bounded; on expiry the CTA records TRSM_ERR_DEVICE_TIMEOUT,
+// lets its copies in flight land and returns.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
-#include "gemm_sp.cuh"  // cp_async16_zfill
-#include "mbarrier.cuh"  // record_timeout
+#include "internal.h"
+#include "mbarrier.cuh"
 
 namespace trsm {
 
-constexpr int kFewNB = 128;   // block rows of the few-RHS path
-constexpr int kFewMaxN = 8;   // right-hand sides it takes
+// right-hand sides it takes: kFewMaxN (internal.h, with the workspace size)
+
+// Block rows: 128.  (256 halves the chain of block rows, but then the tile
+// and W_t a step needs -- 512 KB in f32 -- no longer fit on chip ahead of
+// x_s, and streaming them lengthens every step: measured slower.)
+template <typename T>
+constexpr int few_nb() {
+    return (int)kFewNb;
+}
 
 template <typename T>
 struct FewCfg {
-    static constexpr int KC = 32;                                  // columns of a streamed chunk
-    static constexpr int kChunk = kFewNB * KC;                     // elements
-    static constexpr int ST = sizeof(T) >= 16 ? 3 : 4;             // ring stages
-    static constexpr int VE = 16 / (int)sizeof(T) > 0 ? 16 / (int)sizeof(T) : 1;  // elements per 16 bytes
-    static constexpr size_t kSmem =
-        (size_t)ST * kChunk * sizeof(T) + 2 * (size_t)kFewNB * kFewMaxN * sizeof(T);
+    static constexpr int NB = few_nb<T>();
+    static constexpr int HALVES = 256 / NB;                         // consumer threads per row
+    static constexpr int Q = (int)sizeof(T) / 4;                    // floats per element
+    static constexpr int BR = 256 / Q < NB ? 256 / Q : NB;          // rows per tensor-copy box
+    static constexpr int KC = 32768 / (NB * (int)sizeof(T));        // columns per 32 KB chunk
+    static constexpr int KPT = NB / KC;                             // chunks per tile
+    static constexpr int kChunk = NB * KC;                          // elements per chunk
+    static constexpr int XS = sizeof(T) >= 16 ? 2 : 4;              // x slots
+    static constexpr int kSlot = NB * kFewMaxN;                     // elements per x slot (and rbuf, part)
+    static constexpr size_t kFixed = (size_t)(XS + 2) * kSlot * sizeof(T);
+    static constexpr int ST = (int)((220 * 1024 - kFixed) / (kChunk * sizeof(T)));  // ring stages
+    static constexpr size_t kSmem = (size_t)ST * kChunk * sizeof(T) + kFixed + 1024;
+    static_assert(KC * NB * (int)sizeof(T) == 32768 && KPT >= 2 && KC % (2 * HALVES) == 0, "32 KB chunks");
+    static_assert(ST >= 3, "ring depth");
 };
 
 __device__ __forceinline__ float add2_(float a, float b) { return a + b; }
@@ -42,137 +68,173 @@ __device__ __forceinline__ double add2_(double a, double b) { return a + b; }
 __device__ __forceinline__ float2 add2_(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 __device__ __forceinline__ double2 add2_(double2 a, double2 b) { return make_double2(a.x + b.x, a.y + b.y); }
 
-__device__ __forceinline__ int ld_acquire_flag(const int *p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_flag(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
-}
+// Publication of x_t without a separate flag: the published copy starts as
+// all-ones words (memset before the launch), a pattern no arithmetic result
+// takes (NaNs are stored in canonical form), and every word is written once,
+// by a single store, so a reader that sees no all-ones word has the values.
+// That saves the flag's round trip on the chain of block rows.
+__device__ __forceinline__ bool unset_word(float v) { return __float_as_uint(v) == 0xffffffffu; }
+__device__ __forceinline__ bool unset_word(double v) { return __double_as_longlong(v) == -1ll; }
+__device__ __forceinline__ bool is_unset(float v) { return unset_word(v); }
+__device__ __forceinline__ bool is_unset(double v) { return unset_word(v); }
+__device__ __forceinline__ bool is_unset(float2 v) { return unset_word(v.x) || unset_word(v.y); }
+__device__ __forceinline__ bool is_unset(double2 v) { return unset_word(v.x) || unset_word(v.y); }
+__device__ __forceinline__ float canon(float v) { return v != v ? __uint_as_float(0x7fffffffu) : v; }
+__device__ __forceinline__ double canon(double v) { return v != v ? __longlong_as_double(0x7fffffffffffffffll) : v; }
+__device__ __forceinline__ float2 canon(float2 v) { return make_float2(canon(v.x), canon(v.y)); }
+__device__ __forceinline__ double2 canon(double2 v) { return make_double2(canon(v.x), canon(v.y)); }
+__device__ __forceinline__ float load_fresh(const float *p) { return __ldcv(p); }
+__device__ __forceinline__ double load_fresh(const double *p) { return __ldcv(p); }
+__device__ __forceinline__ float2 load_fresh(const float2 *p) { return __ldcv(p); }
+__device__ __forceinline__ double2 load_fresh(const double2 *p) { return __ldcv(p); }
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
-// 256 threads: thread (row, half) = (tid % 128, tid / 128); a chunk's KC
-// columns are split between the two halves, whose partial sums meet in
-// shared memory at the end of each block row.
 // NC: right-hand sides the registers and loops are sized for (n <= NC; the
 // launcher picks the smallest of 1, 2, 4, 8): a guarded loop over a fixed
 // eight would still issue the idle columns' FMAs, which on the FP64 pipe
 // cost as much as the real ones.
 template <typename T, int NC>
-__global__ void __launch_bounds__(256, 1)
-    few_rhs_kernel(const T *__restrict__ L, int64_t lda, int64_t m, int n, T *B, int64_t ldb,
-                   const T *__restrict__ W, const T alpha, int *flags, int *status, const int64_t wait_limit) {
+__global__ void __launch_bounds__(320, 1)
+    few_rhs_kernel(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapW, int64_t m,
+                   int n, T *B, int64_t ldb, const T alpha, T *xpub, int *status, const int64_t poll_limit) {
     using C = FewCfg<T>;
-    constexpr int NB = kFewNB, KC = C::KC, ST = C::ST, VE = C::VE, KPT = NB / KC;
+    constexpr int NB = C::NB, KC = C::KC, KPT = C::KPT, ST = C::ST, XS = C::XS, BR = C::BR, Q = C::Q;
+    constexpr int HALVES = C::HALVES, KH = KC / HALVES;  // columns of a chunk per thread
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    T *ring = reinterpret_cast<T *>(smem_raw);  // [ST][KC][NB], column j of a chunk at j*NB
-    T *xs = ring + ST * C::kChunk;              // [NB][kFewMaxN]: x_s of the current tile, or r_t
-    T *part = xs + NB * kFewMaxN;               // [NB][kFewMaxN]: the second half's partial sums
-    __shared__ int abort_flag;
-    const int tid = threadIdx.x, row = tid % NB, half = tid / NB;
+    __shared__ __align__(8) uint64_t full[ST], empty[ST], xfull[XS], xempty[XS];
+    __shared__ volatile int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    T *ring = reinterpret_cast<T *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));  // [ST][chunk]
+    T *xs = ring + ST * C::kChunk;                                                  // [XS][NB][8]
+    T *rbuf = xs + XS * C::kSlot;                                                   // [NB][8]: r_t
+    T *part = rbuf + C::kSlot;                                                      // [NB][8]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t tb = (m + NB - 1) / NB;
-    if (tid == 0) abort_flag = 0;
+    if (tid == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 8);
+        }
+        for (int s = 0; s < XS; ++s) {
+            mbar_init(smem_u32(&xfull[s]), 1);
+            mbar_init(smem_u32(&xempty[s]), 8);
+        }
+        abort_flag = 0;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncthreads();
 
-    for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
-        const int64_t r0 = t * NB;
-        const int64_t nchunks = (t + 1) * KPT;  // tiles s < t of L, then W_t
-        // chunk c: columns k0..k0+KC of tile c / KPT, rows r0..r0+NB (zero past m)
-        auto issue = [&](int64_t c) {
-            const int64_t s = c / KPT;
-            const int k0 = (int)(c % KPT) * KC;
-            T *dst = ring + (c % ST) * C::kChunk;
-            const T *src;
-            int64_t ld;
-            int64_t rows_valid;
-            if (s < t) {
-                src = L + (s * NB + k0) * lda + r0;
-                ld = lda;
-                rows_valid = m - r0;
-            } else {
-                src = W + t * NB * NB + (int64_t)k0 * NB;
-                ld = NB;
-                rows_valid = NB;
-            }
-            constexpr int kVecs = KC * NB / VE;
-            for (int e = tid; e < kVecs; e += 256) {
-                const int j = e / (NB / VE), i0 = (e % (NB / VE)) * VE;
-                int bytes = 0;
-                if (i0 < rows_valid) bytes = (int)((rows_valid - i0 < VE ? rows_valid - i0 : VE) * sizeof(T));
-                cp_async16_zfill(dst + j * NB + i0, bytes ? src + j * ld + i0 : src, bytes);
-            }
-        };
-        for (int c = 0; c < ST - 1; ++c) {
-            if (c < nchunks) issue(c);
-            cp_async_commit();
-        }
-        T acc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = zero_of<T>();
-
-        for (int64_t c = 0; c < nchunks; ++c) {
-            const int64_t s = c / KPT;
-            if (c % KPT == 0) {
-                if (s < t) {
-                    // x_s, once its owner has published it
-                    if (tid == 0) {
-                        int64_t spins = 0;
-                        while (ld_acquire_flag(flags + s) == 0) {
-                            if (++spins > wait_limit) {
-                                record_timeout(status);
-                                abort_flag = 1;
-                                break;
-                            }
-                            __nanosleep(64);
-                        }
-                    }
-                    __syncthreads();
-                    if (abort_flag) {
-                        cp_async_wait_all();
-                        return;
-                    }
-                    for (int e = tid; e < NB * NC; e += 256) {
-                        const int i = e / NC, cc = e % NC;
-                        xs[i * kFewMaxN + cc] = cc < n ? __ldcg(B + cc * ldb + s * NB + i) : zero_of<T>();
-                    }
-                } else {
-                    // every tile is in: r_t = alpha b_t - sum_s L_ts x_s
-                    if (half == 1) {
-#pragma unroll
-                        for (int cc = 0; cc < NC; ++cc)
-                            if (cc < n) part[row * kFewMaxN + cc] = acc[cc];
-                    }
-                    __syncthreads();
-                    if (half == 0) {
-#pragma unroll
-                        for (int cc = 0; cc < NC; ++cc) {
-                            if (cc >= n) continue;
-                            const T b = (r0 + row < m) ? B[cc * ldb + r0 + row] : zero_of<T>();
-                            xs[row * kFewMaxN + cc] = sub_(sub_(mul(alpha, b), acc[cc]), part[row * kFewMaxN + cc]);
-                        }
-#pragma unroll
-                        for (int cc = 0; cc < NC; ++cc)
-                            if (cc >= n) xs[row * kFewMaxN + cc] = zero_of<T>();
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
+    if (warp == 0) {
+        // ---------------------------------------------------------- copies
+        if (lane != 0) return;
+        int64_t g = 0;  // chunks issued
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tb && ok; t += gridDim.x) {
+            const int64_t nch = (t + 1) * KPT;  // tiles s < t of L, then W_t
+            for (int64_t c = 0; c < nch; ++c, ++g) {
+                const int stage = (int)(g % ST);
+                if ((g >= ST && !mbar_wait(smem_u32(&empty[stage]), (uint32_t)((g / ST - 1) & 1))) ||
+                    abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bar = smem_u32(&full[stage]);
+                mbar_expect_tx(bar, (uint32_t)(C::kChunk * sizeof(T)));
+                const int64_t s = c / KPT;
+                const int k0 = (int)(c % KPT) * KC;
+                const uint32_t dst = smem_u32(ring + stage * C::kChunk);
+                for (int b = 0; b < NB / BR; ++b) {
+                    // box b: rows b*BR.. of the chunk, KC columns, at b*BR*KC elements
+                    const uint32_t d = dst + (uint32_t)(b * BR * KC * (int)sizeof(T));
+                    if (s < t)
+                        tma_load_3d(d, &mapL, (int)((t * NB + b * BR) * Q), (int)(s * NB + k0), 0, bar);
+                    else
+                        tma_load_3d(d, &mapW, b * BR * Q, (int)(t * NB + k0), 0, bar);
                 }
             }
-            cp_async_wait<ST - 2>();
-            __syncthreads();
-            if (c + ST - 1 < nchunks) issue(c + ST - 1);
-            cp_async_commit();
-            const T *ch = ring + (c % ST) * C::kChunk;
-            const int k0 = (int)(c % KPT) * KC;
-            // two partial sums per column (even / odd j): independent FMA chains
+        }
+        if (!ok) {
+            // the copies issued last may still be landing: wait for them
+            record_timeout(status);
+            abort_flag = 1;
+            for (int64_t h = (g > ST ? g - ST : 0); h < g; ++h)
+                mbar_wait(smem_u32(&full[h % ST]), (uint32_t)((h / ST) & 1));
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // ---------------------------------------------------------- x_s
+        int64_t gx = 0;
+        for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
+            for (int64_t s = 0; s < t; ++s, ++gx) {
+                const int slot = (int)(gx % XS);
+                bool ok = true;
+                if (gx >= XS) ok = mbar_wait(smem_u32(&xempty[slot]), (uint32_t)((gx / XS - 1) & 1));
+                // poll the published x_s (column cc at xpub[(s n + cc) NB ..])
+                // until no word is unset
+                T *dst = xs + slot * C::kSlot;
+                const T *src = xpub + s * (int64_t)n * NB;
+                int64_t polls = 0;
+                while (ok) {
+                    bool mine = true;
+                    for (int e = lane; e < NB * NC; e += 32) {
+                        const int cc = e / NB, i = e % NB;
+                        T v = zero_of<T>();
+                        if (cc < n) {
+                            v = load_fresh(src + cc * NB + i);
+                            if (is_unset(v)) mine = false;
+                        }
+                        dst[i * kFewMaxN + cc] = v;
+                    }
+                    if (__all_sync(0xffffffffu, mine)) break;
+                    if (++polls > poll_limit || abort_flag) ok = false;
+                }
+                if (!ok || abort_flag) {
+                    if (lane == 0) {
+                        record_timeout(status);
+                        abort_flag = 1;
+                    }
+                    return;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&xfull[slot]));
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consume
+    // Every consumer warp runs the same sequence of stage releases and
+    // consumer barriers whatever happens: after a failed wait (abort_flag set)
+    // the warps stop waiting and computing and only walk the sequence, so the
+    // barriers still match; the copy warp stops issuing once it sees abort_flag
+    // and waits for the copies it has in flight before it returns.
+    const int ct = tid - 64, row = ct % NB, half = ct / NB;  // half = 0 when a thread owns a whole row
+    const bool wl = lane == 0;
+    int64_t g = 0, gx = 0;
+    auto fail = [&]() {
+        if (!abort_flag) {
+            record_timeout(status);
+            abort_flag = 1;
+        }
+    };
+    // one chunk of the ring into acc: columns k0.. of the x source
+    auto chunk = [&](const T *__restrict__ xsrc, int k0, T (&acc)[NC]) {
+        const int stage = (int)(g % ST);
+        if (!abort_flag && !mbar_wait(smem_u32(&full[stage]), (uint32_t)((g / ST) & 1))) fail();
+        if (!abort_flag) {
+            const T *ch = ring + stage * C::kChunk;
             T acc2[NC];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc2[cc] = zero_of<T>();
+            // element (r, j) of a chunk: box r / BR, column j, row r % BR
+            const T *base = ch + (row / BR) * BR * KC + row % BR;
 #pragma unroll 4
-            for (int jj = 0; jj < KC / 2; jj += 2) {
-                const int j = half * (KC / 2) + jj;
-                const T a0 = ch[j * NB + row], a1 = ch[(j + 1) * NB + row];
-                const T *xk = xs + (k0 + j) * kFewMaxN;
+            for (int jj = 0; jj < KH; jj += 2) {
+                const int j = half * KH + jj;
+                const T a0 = base[j * BR], a1 = base[(j + 1) * BR];
+                const T *xk = xsrc + (k0 + j) * kFewMaxN;
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) {
                     acc[cc] = fma_(a0, xk[cc], acc[cc]);
@@ -182,30 +244,73 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], acc2[cc]);
         }
-        // x_t = W_t r_t: the halves meet, X goes over b_t, then the flag
-        __syncthreads();
-        if (half == 1) {
+        __syncwarp();
+        if (wl) mbar_arrive(smem_u32(&empty[stage]));
+        ++g;
+    };
+    for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
+        const int64_t r0 = t * NB;
+        // alpha b_t, loaded now: off the chain of block rows
+        T ab[NC];
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc)
+            ab[cc] = (half == 0 && cc < n && r0 + row < m) ? mul(alpha, B[cc * ldb + r0 + row]) : zero_of<T>();
+        T acc[NC];
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
+        for (int64_t s = 0; s < t; ++s, ++gx) {
+            const int slot = (int)(gx % XS);
+            if (!abort_flag && !mbar_wait(smem_u32(&xfull[slot]), (uint32_t)((gx / XS) & 1))) fail();
+            for (int kc = 0; kc < KPT; ++kc) chunk(xs + slot * C::kSlot, kc * KC, acc);
+            __syncwarp();
+            if (wl) mbar_arrive(smem_u32(&xempty[slot]));
+        }
+        // every tile is in: r_t = alpha b_t - sum_s L_ts x_s
+        if (HALVES == 2) {
+            if (half == 1) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) part[row * kFewMaxN + cc] = acc[cc];
+            }
+            consumer_sync();
+            if (half == 0) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], part[row * kFewMaxN + cc]);
+            }
+        }
+        if (half == 0) {
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc)
-                if (cc < n) part[row * kFewMaxN + cc] = acc[cc];
+                rbuf[row * kFewMaxN + cc] = (cc < n && r0 + row < m) ? sub_(ab[cc], acc[cc]) : zero_of<T>();
         }
-        __syncthreads();
+        consumer_sync();
+        // x_t = W_t r_t
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
+        for (int kc = 0; kc < KPT; ++kc) chunk(rbuf, kc * KC, acc);
+        if (HALVES == 2) {
+            if (half == 1) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) part[row * kFewMaxN + cc] = acc[cc];
+            }
+            consumer_sync();
+            if (half == 0) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], part[row * kFewMaxN + cc]);
+            }
+        }
+        // X over b_t, and the published copy for the block rows below (also
+        // after a failure -- the status word then says the result is void --
+        // so that the CTAs waiting on it finish instead of timing out)
         if (half == 0 && r0 + row < m) {
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                if (cc >= n) continue;
-                const T p = part[row * kFewMaxN + cc];
-                B[cc * ldb + r0 + row] = fma_(one_of<T>(), p, acc[cc]);
-            }
-            __threadfence();  // x_t visible GPU-wide before the flag
+            for (int cc = 0; cc < NC; ++cc)
+                if (cc < n) {
+                    B[cc * ldb + r0 + row] = acc[cc];
+                    xpub[(t * n + cc) * NB + row] = canon(acc[cc]);
+                }
         }
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            st_release_flag(flags + t, 1);
-        }
+        consumer_sync();
     }
-    cp_async_wait_all();
 }
 
 template <typename T>

@@ -82,12 +82,25 @@ inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 // tc_fused_bytes_c64, when that form applies and needs more).
 size_t tc_panel_bytes(int64_t m, int64_t n, int64_t nb);
 size_t tc_panel_bytes_c64(int64_t m, int64_t n, int64_t nb);
+// The few-right-hand-sides path (n <= kFewMaxN, few_rhs.cuh) keeps its own
+// data in the same workspace: the inverted diagonal blocks of kFewNb rows,
+// then the published copy of X (block row by block row, column by column).
+constexpr int64_t kFewNb = 128;
+constexpr int kFewMaxN = 8;
+inline size_t few_rhs_bytes(int elem_bytes, int64_t m, int64_t n) {
+    const int64_t tb = (m + kFewNb - 1) / kFewNb;
+    return (size_t)(round256(tb * kFewNb * kFewNb * elem_bytes) + round256(tb * n * kFewNb * elem_bytes));
+}
 inline size_t blocked_workspace_bytes(int dtype, int64_t m, int64_t n, int64_t nb) {
     const int elem_bytes = dtype == 0 ? 4 : dtype == 3 ? 16 : 8;
     const int64_t tb = (m + nb - 1) / nb;
     size_t b = (size_t)(round256(tb * nb * nb * elem_bytes) + 2 * round256(nb * panel_ld(n) * elem_bytes));
     if (dtype == 0) b += tc_panel_bytes(m, n, nb);
     if (dtype == 2) b += tc_panel_bytes_c64(m, n, nb);
+    if (n <= kFewMaxN) {
+        const size_t f = few_rhs_bytes(elem_bytes, m, n);
+        if (f > b) b = f;
+    }
     return b;
 }
 
