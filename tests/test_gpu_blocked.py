@@ -181,7 +181,8 @@ def test_few_rhs_persistent_path(env, dtype, m, n):
     side kernel (one CTA per 128-row block row, each publishing its x_t to
     the CTAs below), ragged last block rows, complex alpha, padded leading
     dimensions; the device status word stays clear, and the phase times show
-    that this kernel ran (no separate applies)."""
+    that this kernel ran (no separate applies; complex128 from three columns
+    on takes the blocked path)."""
     torch, tg = env["torch"], env["tg"]
     per16 = {"f32": 4, "f64": 2, "c64": 2, "c128": 1}[dtype]  # elements in 16 bytes
     lda = (m + per16 - 1) // per16 * per16 + per16           # padded, every column 16-byte aligned
@@ -196,7 +197,10 @@ def test_few_rhs_persistent_path(env, dtype, m, n):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     ms = tg.trsm_llnn_profile(dtype, m, n, alpha, tA, geo["lda"], tB, geo["ldb"], 0, ws, ws_bytes)
-    assert ms[1] == 0.0 and ms[2] > 0.0, f"few-rhs {dtype} m={m} n={n}: phases {ms}"
+    if dtype == "c128" and n > 2:   # complex128 keeps three or more columns on the blocked path
+        assert ms[1] > 0.0, f"blocked {dtype} m={m} n={n}: phases {ms}"
+    else:
+        assert ms[1] == 0.0 and ms[2] > 0.0, f"few-rhs {dtype} m={m} n={n}: phases {ms}"
     assert_parity(dtype, logical(tB.cpu().numpy(), geo), xr, f"few-rhs profiled {dtype} m={m} n={n}")
 
 

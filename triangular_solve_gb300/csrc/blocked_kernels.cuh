@@ -210,6 +210,136 @@ constexpr size_t inv_offdiag_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// One CTA (256 threads) inverts a whole 128 x 128 diagonal block D_t in
+// shared memory, for the few-right-hand-side path: the two kernels above
+// (sub-blocks in CTAs of I_B threads, then the off-diagonal sub-blocks one
+// after another) are latency-bound at NB = 128.  The same blocked
+// triangular-inverse formula, level by level, in place:
+//   level 1  warps 0-3 invert the four 32 x 32 diagonal sub-blocks by
+//            substitution against identity columns (lane j: column j, in
+//            registers, column k of the sub-block read as a broadcast);
+//   level 2  each 64 x 64 diagonal block [[A, 0], [C, B]], A^{-1} and B^{-1}
+//            known, gets its lower-left block -B^{-1} (C A^{-1}): two
+//            products, the middle one in a temporary;
+//   level 3  the same for the whole block with 64 x 64 parts.
+// The products skip the zero triangles of A^{-1} and B^{-1}.  Rows and
+// columns at or beyond m are identity padding; the strictly upper triangle
+// is zero.  Output W_t: 128 x 128, column-major, ld 128, at W + t 128^2.
+// Used for f32 and c64 (the block and a 64 x 64 temporary fit the 227 KB
+// up to 8-byte elements; in f64 one SM's FP64 rate makes the two-kernel
+// inversion, spread over more CTAs, the faster one).
+// ---------------------------------------------------------------------------
+constexpr int kInvN = 128, kInvLd = kInvN + 1, kInvTmpLd = 65;
+
+template <typename T>
+constexpr size_t inv_block128_smem() {
+    return sizeof(T) * ((size_t)kInvN * kInvLd + (size_t)64 * kInvTmpLd);
+}
+
+// C = (NEG ? -1 : 1) A B over R x R parts (column-major, leading dimensions
+// la, lb, lc); A lower triangular when A_LOWER, B when B_LOWER.  Thread lt of
+// the (R/PR)(R/PC) taking part owns rows i0 .. i0+PR-1, columns j0 .. j0+PC-1.
+template <typename T, int R, int PR, int PC, bool A_LOWER, bool B_LOWER, bool NEG>
+__device__ __forceinline__ void inv_part_product(const T *A, int la, const T *Bm, int lb, T *Cm, int lc, int lt) {
+    const int i0 = (lt % (R / PR)) * PR, j0 = (lt / (R / PR)) * PC;
+    T acc[PR][PC];
+#pragma unroll
+    for (int x = 0; x < PR; ++x)
+#pragma unroll
+        for (int y = 0; y < PC; ++y) acc[x][y] = zero_of<T>();
+    const int k_lo = B_LOWER ? j0 : 0;               // B(k, j) = 0 for k < j
+    const int k_hi = A_LOWER ? i0 + PR : R;          // A(i, k) = 0 for k > i
+#pragma unroll 2
+    for (int k = k_lo; k < k_hi; ++k) {
+        T a[PR], b[PC];
+#pragma unroll
+        for (int x = 0; x < PR; ++x) a[x] = A[k * la + i0 + x];
+#pragma unroll
+        for (int y = 0; y < PC; ++y) b[y] = Bm[(j0 + y) * lb + k];
+#pragma unroll
+        for (int x = 0; x < PR; ++x)
+#pragma unroll
+            for (int y = 0; y < PC; ++y) acc[x][y] = NEG ? fms(a[x], b[y], acc[x][y]) : fma_(a[x], b[y], acc[x][y]);
+    }
+#pragma unroll
+    for (int x = 0; x < PR; ++x)
+#pragma unroll
+        for (int y = 0; y < PC; ++y) Cm[(j0 + y) * lc + i0 + x] = acc[x][y];
+}
+
+// fill (optional): fill_words 32-bit words per CTA set to all ones, at
+// fill + blockIdx.x fill_words (the few-right-hand-side path's published copy
+// of X, cleared here instead of by a separate memset).
+template <typename T>
+__global__ void __launch_bounds__(256) inv_block128_kernel(const T *__restrict__ L, int64_t lda, int64_t m,
+                                                           T *__restrict__ W, uint32_t *__restrict__ fill,
+                                                           int64_t fill_words) {
+    extern __shared__ __align__(16) unsigned char inv_smem[];
+    T *S = reinterpret_cast<T *>(inv_smem);  // D_t, then W_t: element (i, j) at j kInvLd + i
+    T *Tmp = S + kInvN * kInvLd;             // 64 x 64 (or two 32 x 32), ld kInvTmpLd
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t r0 = (int64_t)blockIdx.x * kInvN;
+    const int mb = (int)(m - r0 < kInvN ? m - r0 : kInvN);
+    {
+        // thread: row i of columns j0, j0 + 2, ..., 32 loads in flight at a time
+        const int i = tid % kInvN, j0 = tid / kInvN;
+#pragma unroll 1
+        for (int q0 = 0; q0 < kInvN / 2; q0 += 32) {
+            T v[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int j = j0 + 2 * (q0 + q);
+                v[q] = (i >= j && i < mb) ? L[(r0 + j) * lda + r0 + i] : (i == j ? one_of<T>() : zero_of<T>());
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) S[(j0 + 2 * (q0 + q)) * kInvLd + i] = v[q];
+        }
+    }
+    __syncthreads();
+    if (warp < 4) {
+        // level 1: lane j solves D_ww y = e_j for the sub-block at rows and
+        // columns 32 warp ..; right-looking, y_k final at step k
+        T *D = S + warp * 32 * (kInvLd + 1);
+        T y[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = i == lane ? one_of<T>() : zero_of<T>();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const T *col = D + k * kInvLd;
+            y[k] = mul(y[k], recip(col[k]));
+#pragma unroll
+            for (int i = k + 1; i < 32; ++i) y[i] = fms(col[i], y[k], y[i]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) D[lane * kInvLd + i] = y[i];
+    }
+    __syncthreads();
+    {
+        // level 2: the two 64 x 64 diagonal blocks at o = 0, 64, 128 threads each
+        const int o = (tid >> 7) * 64, lt = tid & 127;
+        T *A = S + o * kInvLd + o, *Bi = S + (o + 32) * kInvLd + o + 32, *C = S + o * kInvLd + o + 32;
+        T *P = Tmp + (tid >> 7) * 32 * kInvTmpLd;
+        inv_part_product<T, 32, 4, 2, false, true, false>(C, kInvLd, A, kInvLd, P, kInvTmpLd, lt);
+        __syncthreads();
+        inv_part_product<T, 32, 4, 2, true, false, true>(Bi, kInvLd, P, kInvTmpLd, C, kInvLd, lt);
+        __syncthreads();
+    }
+    {
+        // level 3: the whole block, 64 x 64 parts
+        T *A = S, *Bi = S + 64 * kInvLd + 64, *C = S + 64;
+        inv_part_product<T, 64, 4, 4, false, true, false>(C, kInvLd, A, kInvLd, Tmp, kInvTmpLd, tid);
+        __syncthreads();
+        inv_part_product<T, 64, 4, 4, true, false, true>(Bi, kInvLd, Tmp, kInvTmpLd, C, kInvLd, tid);
+        __syncthreads();
+    }
+    T *Wt = W + (int64_t)blockIdx.x * kInvN * kInvN;
+    for (int e = tid; e < kInvN * kInvN; e += 256) Wt[e] = S[(e / kInvN) * kInvLd + e % kInvN];
+    if (fill)
+        for (int64_t e = tid; e < fill_words; e += 256) fill[(int64_t)blockIdx.x * fill_words + e] = 0xffffffffu;
+}
+
+// ---------------------------------------------------------------------------
 // Tiled GEMM  C = beta*C + gamma * A * B  (all column-major; beta_zero skips
 // reading C).  With a_lower, A is lower triangular and the K loop of a
 // row tile stops at the tile's last row.  256 threads, a TM x TN register

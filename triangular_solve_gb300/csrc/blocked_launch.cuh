@@ -163,9 +163,13 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
 // workspace of ws_bytes.
 constexpr int64_t kFewMinM = 512;
 
+// complex128 only up to two columns: from three on, each block row's FP64
+// work on the chain (one SM) outweighs what the kernel saves, and the
+// blocked path is as fast or faster.
 template <typename T>
 static bool few_rhs_usable(int64_t m, int64_t n, const T *L, int64_t lda, size_t ws_bytes) {
-    return n >= 1 && n <= kFewMaxN && m > kFewMinM && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) &&
+    const int64_t max_n = std::is_same<T, double2>::value ? 2 : kFewMaxN;
+    return n >= 1 && n <= max_n && m > kFewMinM && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) &&
            (lda * (int64_t)sizeof(T)) % 16 == 0 && few_rhs_bytes((int)sizeof(T), m, n) <= ws_bytes;
 }
 
@@ -198,9 +202,24 @@ static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, in
     if (inv_ms)
         for (auto &x : e) cudaEventCreate(&x);
     if (inv_ms) cudaEventRecord(e[0], st);
-    int rc = invert_diagonal_blocks<T, (int)NB / 8>(L, lda, m, (int)NB, W, st);
-    // every word of the published copy unset (all ones) until written
-    if (!rc) rc = cuda_status(cudaMemsetAsync(xpub, 0xff, (size_t)(tb * n * NB) * sizeof(T), st));
+    // every word of the published copy of X unset (all ones) until written
+    int rc = TRSM_SUCCESS;
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
+        // one CTA per diagonal block, the whole block in shared memory; it
+        // also clears its block row of the published copy
+        constexpr size_t ismem = inv_block128_smem<T>();
+        static_assert(NB == kInvN, "block rows of 128");
+        rc = cuda_status(cudaFuncSetAttribute(inv_block128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)ismem));
+        if (!rc) {
+            inv_block128_kernel<T><<<(unsigned)tb, 256, ismem, st>>>(
+                L, lda, m, W, reinterpret_cast<uint32_t *>(xpub), n * NB * (int64_t)sizeof(T) / 4);
+            rc = launch_status();
+        }
+    } else {
+        rc = invert_diagonal_blocks<T, (int)NB / 8>(L, lda, m, (int)NB, W, st);
+        if (!rc) rc = cuda_status(cudaMemsetAsync(xpub, 0xff, (size_t)(tb * n * NB) * sizeof(T), st));
+    }
     int *status = nullptr;
     if (!rc) rc = device_status_word(&status);
     if (inv_ms) cudaEventRecord(e[1], st);

@@ -20,9 +20,11 @@
 //             columns at a time, into a ring of mbarrier-tracked stages;
 //   warp 1    polls each block row's published x_s and stages it in a small
 //             ring of slots, a few tiles ahead of the consumers;
-//   warps 2-9 consume: thread (row, half) accumulates its row of L_ts x_s
-//             over half of each chunk's columns; the two halves meet in
-//             shared memory once per block row.
+//   warps 2-9 consume: two threads a row, each accumulating its row of
+//             L_ts x_s over half of each chunk's columns; the halves meet
+//             once per product in shared memory.  In f32 with n = 1 the
+//             tile on the chain, L_{t,t-1}, and W_t are moved to registers
+//             before x_{t-1} arrives.
 // Every wait is bounded; on expiry the CTA records TRSM_ERR_DEVICE_TIMEOUT,
 // lets its copies in flight land and returns.
 #pragma once
@@ -60,6 +62,7 @@ struct FewCfg {
     static constexpr int ST = (int)((220 * 1024 - kFixed) / (kChunk * sizeof(T)));  // ring stages
     static constexpr size_t kSmem = (size_t)ST * kChunk * sizeof(T) + kFixed + 1024;
     static_assert(KC * NB * (int)sizeof(T) == 32768 && KPT >= 2 && KC % (2 * HALVES) == 0, "32 KB chunks");
+    static_assert(HALVES == 2, "two threads a row");
     static_assert(ST >= 3, "ring depth");
 };
 
@@ -83,10 +86,57 @@ __device__ __forceinline__ float canon(float v) { return v != v ? __uint_as_floa
 __device__ __forceinline__ double canon(double v) { return v != v ? __longlong_as_double(0x7fffffffffffffffll) : v; }
 __device__ __forceinline__ float2 canon(float2 v) { return make_float2(canon(v.x), canon(v.y)); }
 __device__ __forceinline__ double2 canon(double2 v) { return make_double2(canon(v.x), canon(v.y)); }
-__device__ __forceinline__ float load_fresh(const float *p) { return __ldcv(p); }
-__device__ __forceinline__ double load_fresh(const double *p) { return __ldcv(p); }
-__device__ __forceinline__ float2 load_fresh(const float2 *p) { return __ldcv(p); }
-__device__ __forceinline__ double2 load_fresh(const double2 *p) { return __ldcv(p); }
+// The published copy is written and polled with relaxed gpu-scope accesses:
+// a plain load in a polling loop may legally be hoisted out of it (another
+// thread's store is then a data race), a relaxed one may not, and it reads
+// the L2's current value.  Each component is one single-copy-atomic access.
+__device__ __forceinline__ float load_fresh(const float *p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ double load_fresh(const double *p) {
+    double v;
+    asm volatile("ld.relaxed.gpu.global.f64 %0, [%1];\n" : "=d"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 load_fresh(const float2 *p) {
+    float2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ double2 load_fresh(const double2 *p) {
+    double2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.f64 {%0, %1}, [%2];\n" : "=d"(v.x), "=d"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void store_published(float *p, float v) {
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;\n" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void store_published(double *p, double v) {
+    asm volatile("st.relaxed.gpu.global.f64 [%0], %1;\n" ::"l"(p), "d"(v) : "memory");
+}
+__device__ __forceinline__ void store_published(float2 *p, float2 v) {
+    asm volatile("st.relaxed.gpu.global.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ void store_published(double2 *p, double2 v) {
+    asm volatile("st.relaxed.gpu.global.v2.f64 [%0], {%1, %2};\n" ::"l"(p), "d"(v.x), "d"(v.y) : "memory");
+}
+// two consecutive elements of shared memory (8-byte aligned pairs of f32,
+// 16-byte of the others) in one access where the width allows
+__device__ __forceinline__ void load_pair(const float *p, float &a, float &b) {
+    const float2 v = *reinterpret_cast<const float2 *>(p);
+    a = v.x, b = v.y;
+}
+__device__ __forceinline__ void load_pair(const double *p, double &a, double &b) {
+    const double2 v = *reinterpret_cast<const double2 *>(p);
+    a = v.x, b = v.y;
+}
+__device__ __forceinline__ void load_pair(const float2 *p, float2 &a, float2 &b) {
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    a = make_float2(v.x, v.y), b = make_float2(v.z, v.w);
+}
+__device__ __forceinline__ void load_pair(const double2 *p, double2 &a, double2 &b) { a = p[0], b = p[1]; }
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
 // NC: right-hand sides the registers and loops are sized for (n <= NC; the
@@ -99,15 +149,19 @@ __global__ void __launch_bounds__(320, 1)
                    int n, T *B, int64_t ldb, const T alpha, T *xpub, int *status, const int64_t poll_limit) {
     using C = FewCfg<T>;
     constexpr int NB = C::NB, KC = C::KC, KPT = C::KPT, ST = C::ST, XS = C::XS, BR = C::BR, Q = C::Q;
-    constexpr int HALVES = C::HALVES, KH = KC / HALVES;  // columns of a chunk per thread
+    // f32 with one right-hand side holds the tile on the chain and W_t in
+    // registers (see the consumers); W_t then comes first in a block row's
+    // stream
+    constexpr bool kReg = std::is_same<T, float>::value && NC == 1;
+    constexpr int KH = KC / C::HALVES;  // columns of a chunk per thread
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full[ST], empty[ST], xfull[XS], xempty[XS];
     __shared__ volatile int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     T *ring = reinterpret_cast<T *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));  // [ST][chunk]
-    T *xs = ring + ST * C::kChunk;                                                  // [XS][NB][8]
-    T *rbuf = xs + XS * C::kSlot;                                                   // [NB][8]: r_t
-    T *part = rbuf + C::kSlot;                                                      // [NB][8]
+    T *xs = ring + ST * C::kChunk;                                                  // [XS][8][NB]
+    T *rbuf = xs + XS * C::kSlot;                                                   // [8][NB]: r_t
+    T *part = rbuf + C::kSlot;                                                      // [8][NB]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t tb = (m + NB - 1) / NB;
     if (tid == 0) {
@@ -130,7 +184,7 @@ __global__ void __launch_bounds__(320, 1)
         int64_t g = 0;  // chunks issued
         bool ok = true;
         for (int64_t t = blockIdx.x; t < tb && ok; t += gridDim.x) {
-            const int64_t nch = (t + 1) * KPT;  // tiles s < t of L, then W_t
+            const int64_t nch = (t + 1) * KPT;  // tiles s < t of L and W_t (first when kReg, else last)
             for (int64_t c = 0; c < nch; ++c, ++g) {
                 const int stage = (int)(g % ST);
                 if ((g >= ST && !mbar_wait(smem_u32(&empty[stage]), (uint32_t)((g / ST - 1) & 1))) ||
@@ -140,7 +194,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 const uint32_t bar = smem_u32(&full[stage]);
                 mbar_expect_tx(bar, (uint32_t)(C::kChunk * sizeof(T)));
-                const int64_t s = c / KPT;
+                const int64_t s = kReg ? (c < KPT ? t : c / KPT - 1) : c / KPT;
                 const int k0 = (int)(c % KPT) * KC;
                 const uint32_t dst = smem_u32(ring + stage * C::kChunk);
                 for (int b = 0; b < NB / BR; ++b) {
@@ -165,6 +219,9 @@ __global__ void __launch_bounds__(320, 1)
 
     if (warp == 1) {
         // ---------------------------------------------------------- x_s
+        constexpr int kPollE = NB * NC / 32;                        // elements a lane polls
+        constexpr bool kPollTwo = kPollE * sizeof(T) <= 64;         // two polls held in registers
+        constexpr long long kPollGap = 600;                         // cycles, about half an L2 round trip
         int64_t gx = 0;
         for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
             for (int64_t s = 0; s < t; ++s, ++gx) {
@@ -172,23 +229,63 @@ __global__ void __launch_bounds__(320, 1)
                 bool ok = true;
                 if (gx >= XS) ok = mbar_wait(smem_u32(&xempty[slot]), (uint32_t)((gx / XS - 1) & 1));
                 // poll the published x_s (column cc at xpub[(s n + cc) NB ..])
-                // until no word is unset
+                // until no word is unset; lane element q: e = lane + 32 q
                 T *dst = xs + slot * C::kSlot;
                 const T *src = xpub + s * (int64_t)n * NB;
-                int64_t polls = 0;
-                while (ok) {
-                    bool mine = true;
-                    for (int e = lane; e < NB * NC; e += 32) {
-                        const int cc = e / NB, i = e % NB;
-                        T v = zero_of<T>();
-                        if (cc < n) {
-                            v = load_fresh(src + cc * NB + i);
-                            if (is_unset(v)) mine = false;
-                        }
-                        dst[i * kFewMaxN + cc] = v;
+                auto issue = [&](T (&v)[kPollE]) {
+#pragma unroll
+                    for (int q = 0; q < kPollE; ++q) {
+                        const int e = lane + 32 * q, cc = e / NB;
+                        v[q] = cc < n ? load_fresh(src + cc * NB + e % NB) : zero_of<T>();
                     }
-                    if (__all_sync(0xffffffffu, mine)) break;
-                    if (++polls > poll_limit || abort_flag) ok = false;
+                };
+                auto landed = [&](const T (&v)[kPollE]) {
+                    bool mine = true;
+#pragma unroll
+                    for (int q = 0; q < kPollE; ++q) mine = mine && !is_unset(v[q]);
+                    if (!__all_sync(0xffffffffu, mine)) return false;
+#pragma unroll
+                    for (int q = 0; q < kPollE; ++q) {
+                        const int e = lane + 32 * q;
+                        dst[(e / NB) * NB + e % NB] = v[q];
+                    }
+                    return true;
+                };
+                int64_t polls = 0;
+                if constexpr (kPollTwo) {
+                    // two polls in flight, issued about half a round trip
+                    // apart (the first pair split by a short spin, then each
+                    // poll reissued as soon as its check comes back)
+                    T va[kPollE], vb[kPollE];
+                    if (ok) {
+                        issue(va);
+                        const long long t0 = clock64();
+                        while (clock64() - t0 < kPollGap) {
+                        }
+                    }
+                    while (ok) {
+                        issue(vb);
+                        if (landed(va)) break;
+                        issue(va);
+                        if (landed(vb)) break;
+                        if ((polls += 2) > poll_limit || abort_flag) ok = false;
+                    }
+                } else {
+                    // too wide to hold in registers: staged as it is read
+                    while (ok) {
+                        bool mine = true;
+                        for (int e = lane; e < NB * NC; e += 32) {
+                            const int cc = e / NB, i = e % NB;
+                            T v = zero_of<T>();
+                            if (cc < n) {
+                                v = load_fresh(src + cc * NB + i);
+                                if (is_unset(v)) mine = false;
+                            }
+                            dst[cc * NB + i] = v;
+                        }
+                        if (__all_sync(0xffffffffu, mine)) break;
+                        if (++polls > poll_limit || abort_flag) ok = false;
+                    }
                 }
                 if (!ok || abort_flag) {
                     if (lane == 0) {
@@ -210,7 +307,10 @@ __global__ void __launch_bounds__(320, 1)
     // the warps stop waiting and computing and only walk the sequence, so the
     // barriers still match; the copy warp stops issuing once it sees abort_flag
     // and waits for the copies it has in flight before it returns.
-    const int ct = tid - 64, row = ct % NB, half = ct / NB;  // half = 0 when a thread owns a whole row
+    // Two threads per row, each over half of a chunk's columns: a warp
+    // covers 32 rows (conflict-free shared-memory reads of the tiles), the
+    // halves in warps cw and cw + 4, meeting in shared memory.
+    const int ct = tid - 64, row = ct % NB, half = ct / NB;
     const bool wl = lane == 0;
     int64_t g = 0, gx = 0;
     auto fail = [&]() {
@@ -219,7 +319,19 @@ __global__ void __launch_bounds__(320, 1)
             abort_flag = 1;
         }
     };
-    // one chunk of the ring into acc: columns k0.. of the x source
+    // the halves' sums of a row, in half 0
+    auto combine = [&](T (&acc)[NC]) {
+        if (half == 1) {
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) part[cc * NB + row] = acc[cc];
+        }
+        consumer_sync();
+        if (half == 0) {
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], part[cc * NB + row]);
+        }
+    };
+    // one chunk of the ring into acc: columns k0.. of the x source ([cc][NB])
     auto chunk = [&](const T *__restrict__ xsrc, int k0, T (&acc)[NC]) {
         const int stage = (int)(g % ST);
         if (!abort_flag && !mbar_wait(smem_u32(&full[stage]), (uint32_t)((g / ST) & 1))) fail();
@@ -230,15 +342,17 @@ __global__ void __launch_bounds__(320, 1)
             for (int cc = 0; cc < NC; ++cc) acc2[cc] = zero_of<T>();
             // element (r, j) of a chunk: box r / BR, column j, row r % BR
             const T *base = ch + (row / BR) * BR * KC + row % BR;
-#pragma unroll 4
+#pragma unroll(NC >= 4 ? 2 : 4)
             for (int jj = 0; jj < KH; jj += 2) {
                 const int j = half * KH + jj;
                 const T a0 = base[j * BR], a1 = base[(j + 1) * BR];
-                const T *xk = xsrc + (k0 + j) * kFewMaxN;
+                const T *xk = xsrc + k0 + j;
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) {
-                    acc[cc] = fma_(a0, xk[cc], acc[cc]);
-                    acc2[cc] = fma_(a1, xk[kFewMaxN + cc], acc2[cc]);
+                    T x0, x1;
+                    load_pair(xk + cc * NB, x0, x1);
+                    acc[cc] = fma_(a0, x0, acc[cc]);
+                    acc2[cc] = fma_(a1, x1, acc2[cc]);
                 }
             }
 #pragma unroll
@@ -248,6 +362,60 @@ __global__ void __launch_bounds__(320, 1)
         if (wl) mbar_arrive(smem_u32(&empty[stage]));
         ++g;
     };
+    // kReg (f32, n = 1): the tile on the chain (L_{t,t-1}) and W_t go to
+    // registers while x_{t-1} is still on its way (128 of the 168 registers
+    // a thread has with ten warps on an SM), so the chain step reads only x
+    // from shared memory.  Chunk kc holds columns kc KC ..: with KC = NB / 2
+    // this thread's half is exactly chunk `half`.
+    constexpr int HC = kReg ? NB / 2 : 1;
+    static_assert(!kReg || (KC == HC && KPT == 2 && BR == NB), "f32 chunks are column halves");
+    auto preload = [&](T (&R)[HC]) {
+        for (int kc = 0; kc < KPT; ++kc) {
+            const int64_t h = g + kc;
+            if (!abort_flag && !mbar_wait(smem_u32(&full[h % ST]), (uint32_t)((h / ST) & 1))) fail();
+        }
+        if (!abort_flag) {
+            const T *ch = ring + (int)((g + half) % ST) * C::kChunk + row;
+#pragma unroll
+            for (int j = 0; j < HC; ++j) R[j] = ch[j * BR];
+        } else {
+#pragma unroll
+            for (int j = 0; j < HC; ++j) R[j] = zero_of<T>();
+        }
+        __syncwarp();
+        if (wl)
+            for (int kc = 0; kc < KPT; ++kc) mbar_arrive(smem_u32(&empty[(g + kc) % ST]));
+        g += KPT;
+    };
+    // acc += R . src over this thread's half of the columns (src [cc][NB]);
+    // a few partial sums per column keep the FMA chains short
+    auto reg_matvec = [&](const T (&R)[HC], const T *__restrict__ src, T (&acc)[NC]) {
+        if constexpr (kReg) {
+            constexpr int P = NC >= 4 ? 1 : 4 / NC;
+            float p[P][NC];
+#pragma unroll
+            for (int q = 0; q < P; ++q)
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) p[q][cc] = 0.f;
+            const float *xb = src + half * HC;
+#pragma unroll
+            for (int j = 0; j < HC; j += 4) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    const float4 v = *reinterpret_cast<const float4 *>(xb + cc * NB + j);
+                    p[(j / 4 + 0) % P][cc] = fmaf(R[j], v.x, p[(j / 4 + 0) % P][cc]);
+                    p[(j / 4 + 1) % P][cc] = fmaf(R[j + 1], v.y, p[(j / 4 + 1) % P][cc]);
+                    p[(j / 4 + 2) % P][cc] = fmaf(R[j + 2], v.z, p[(j / 4 + 2) % P][cc]);
+                    p[(j / 4 + 3) % P][cc] = fmaf(R[j + 3], v.w, p[(j / 4 + 3) % P][cc]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < P; ++q)
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc[cc] += p[q][cc];
+        }
+    };
+    T Lreg[HC], Wreg[HC];
     for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
         const int64_t r0 = t * NB;
         // alpha b_t, loaded now: off the chain of block rows
@@ -258,46 +426,37 @@ __global__ void __launch_bounds__(320, 1)
         T acc[NC];
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
+        const int64_t s_reg = kReg ? t - 1 : t;  // the tile from registers
+        if (kReg) preload(Wreg);
         for (int64_t s = 0; s < t; ++s, ++gx) {
             const int slot = (int)(gx % XS);
+            if (s == s_reg) preload(Lreg);
             if (!abort_flag && !mbar_wait(smem_u32(&xfull[slot]), (uint32_t)((gx / XS) & 1))) fail();
-            for (int kc = 0; kc < KPT; ++kc) chunk(xs + slot * C::kSlot, kc * KC, acc);
+            if (s == s_reg) {
+                if (!abort_flag) reg_matvec(Lreg, xs + slot * C::kSlot, acc);
+            } else {
+                for (int kc = 0; kc < KPT; ++kc) chunk(xs + slot * C::kSlot, kc * KC, acc);
+            }
             __syncwarp();
             if (wl) mbar_arrive(smem_u32(&xempty[slot]));
         }
         // every tile is in: r_t = alpha b_t - sum_s L_ts x_s
-        if (HALVES == 2) {
-            if (half == 1) {
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc) part[row * kFewMaxN + cc] = acc[cc];
-            }
-            consumer_sync();
-            if (half == 0) {
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], part[row * kFewMaxN + cc]);
-            }
-        }
+        combine(acc);
         if (half == 0) {
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc)
-                rbuf[row * kFewMaxN + cc] = (cc < n && r0 + row < m) ? sub_(ab[cc], acc[cc]) : zero_of<T>();
+                rbuf[cc * NB + row] = sub_(ab[cc], acc[cc]);
         }
         consumer_sync();
         // x_t = W_t r_t
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
-        for (int kc = 0; kc < KPT; ++kc) chunk(rbuf, kc * KC, acc);
-        if (HALVES == 2) {
-            if (half == 1) {
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc) part[row * kFewMaxN + cc] = acc[cc];
-            }
-            consumer_sync();
-            if (half == 0) {
-#pragma unroll
-                for (int cc = 0; cc < NC; ++cc) acc[cc] = add2_(acc[cc], part[row * kFewMaxN + cc]);
-            }
+        if (kReg) {
+            if (!abort_flag) reg_matvec(Wreg, rbuf, acc);
+        } else {
+            for (int kc = 0; kc < KPT; ++kc) chunk(rbuf, kc * KC, acc);
         }
+        combine(acc);
         // X over b_t, and the published copy for the block rows below (also
         // after a failure -- the status word then says the result is void --
         // so that the CTAs waiting on it finish instead of timing out)
@@ -306,10 +465,10 @@ __global__ void __launch_bounds__(320, 1)
             for (int cc = 0; cc < NC; ++cc)
                 if (cc < n) {
                     B[cc * ldb + r0 + row] = acc[cc];
-                    xpub[(t * n + cc) * NB + row] = canon(acc[cc]);
+                    store_published(xpub + (t * n + cc) * NB + row, canon(acc[cc]));
                 }
         }
-        consumer_sync();
+        consumer_sync();  // rbuf and part are rewritten for the next block row
     }
 }
 
