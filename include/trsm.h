@@ -78,8 +78,10 @@ typedef enum { TRSM_NONUNIT = 0, TRSM_UNIT = 1 } trsm_diag_t;
  * as one cooperative persistent launch over 128-row block rows (also through
  * trsm_llnn_ex when its nb is 0 or 128).  The blocked path needs a
  * device workspace of trsm_llnn_workspace_bytes(dtype, m, n, 0) bytes; this
- * entry point allocates it with cudaMallocAsync on `stream` and frees it with
- * cudaFreeAsync on the same stream.  Use trsm_llnn_ex to pass your own.
+ * entry point takes it, ordered on `stream`, from a memory pool the library
+ * keeps per device (cudaMallocFromPoolAsync / cudaFreeAsync; the pool keeps
+ * its memory between calls, up to the largest workspace in use at once).
+ * Use trsm_llnn_ex to pass your own, trsm_llnn_noalloc to allocate nothing.
  *
  * Arguments: 1 dtype, 2 m, 3 n, 4 alpha, 5 A, 6 lda, 7 B, 8 ldb, 9 stream.
  */
@@ -100,8 +102,7 @@ int trsm_llnn(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alpha,
  * every kernel's grid; one inversion for all systems when strideA == 0),
  * chunked to at most 65535 systems and 1 GiB of workspace per chunk.
  * Larger m: the blocked path system by system.  The workspace of the blocked
- * paths is allocated with cudaMallocAsync on `stream` and freed on it, as in
- * trsm_llnn.
+ * paths comes from the library's pool, ordered on `stream`, as in trsm_llnn.
  *
  * Arguments: 1 dtype, 2 layout, 3 m, 4 n, 5 alpha, 6 A, 7 lda, 8 strideA,
  * 9 B, 10 ldb, 11 strideB, 12 batch, 13 stream.
@@ -209,8 +210,8 @@ int trsm_llnn_profile(trsm_dtype_t dtype, int64_t m, int64_t n, const void *alph
  * other is mapped onto it: the matrix of the equivalent left-side lower
  * problem (op(A), or op(A)^T for the right side, reversed in row and column
  * order when it is upper, with the unit diagonal written in) is copied into
- * a stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`,
- * k^2 elements, plus m n for the right side), B is reversed in row order or
+ * a workspace from the library's pool, ordered on `stream` (k^2 elements,
+ * plus m n for the right side), B is reversed in row order or
  * transposed into the workspace around the solve, and trsm_llnn runs on it.
  * alpha = 0 sets B to zero without reading A.  The order of A and the other
  * dimension are limited to 65535 for the variants that copy.

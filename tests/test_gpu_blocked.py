@@ -76,25 +76,39 @@ def test_batched_blocked(env, dtype, layout):
     assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"batched blocked {layout}")
 
 
-def test_inverse_blocks_times_diagonal_blocks_is_identity(env):
+@pytest.mark.parametrize("dtype,m,nb", [
+    ("f64", 1000, 256),
+    ("f32", 1000, 512),   # doubling: 128-row blocks, then 256 and 512; last block 488 rows
+    ("f32", 700, 512),    # last block 188 rows: lower-left blocks past m zeroed
+    ("c64", 1536, 256),   # three full blocks
+    ("c64", 1000, 512),
+    ("f32", 1000, 128),
+])
+def test_inverse_blocks_times_diagonal_blocks_is_identity(env, dtype, m, nb):
     """The inverted diagonal blocks left in the workspace satisfy W_t D_t = I
-    (the identity-tile substitution and the blocked inverse formula)."""
+    and have a zero upper triangle: the identity-tile substitution with the
+    blocked inverse formula (f64), and for f32 / c64 the one-CTA 128-row
+    inversion followed by the doubling products, ragged last blocks
+    included (padding rows and columns are identity)."""
     torch, tg = env["torch"], env["tg"]
-    dtype, m, n, nb = "f64", 1000, 8, 256
+    n = 16   # past the few-right-hand-side path
     L, B = ti.generate(dtype, m, n, 1, kind="ddm")
     a, b, geo = storage_pair(L, B)
     ws_bytes = tg.trsm_llnn_workspace_bytes(dtype, m, n, nb)
-    ws = torch.zeros(ws_bytes // 8, dtype=torch.float64, device="cuda")
+    ws = torch.full((ws_bytes,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN until written
     tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     tg.trsm_llnn_ex(dtype, m, n, 1.0, tA, m, tB, m, nb, ws, ws_bytes)
     torch.cuda.synchronize()
-    W = ws.cpu().numpy()
+    np_t = {"f32": np.float32, "f64": np.float64, "c64": np.complex64, "c128": np.complex128}[dtype]
+    W = ws.cpu().numpy().view(np_t)
+    atol = 1e-13 if dtype == "f64" else 2e-5
     for t in range((m + nb - 1) // nb):
         r0, mb = t * nb, min(nb, m - t * nb)
-        Wt = W[t * nb * nb:(t + 1) * nb * nb].reshape(nb, nb).T[:mb, :mb]   # column-major block
+        Wfull = W[t * nb * nb:(t + 1) * nb * nb].reshape(nb, nb).T   # column-major block
+        Wt = Wfull[:mb, :mb]
         Dt = L[0, r0:r0 + mb, r0:r0 + mb]
-        np.testing.assert_allclose(Wt @ Dt, np.eye(mb), atol=1e-13)
-        assert np.all(np.triu(Wt, 1) == 0)
+        np.testing.assert_allclose(Wt @ Dt, np.eye(mb), atol=atol, err_msg=f"{dtype} m={m} nb={nb} t={t}")
+        assert np.all(np.triu(Wfull, 1) == 0)   # written as zeros, not left over
 
 
 @pytest.mark.parametrize("dtype", ["f64", "c128", "f32"])

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "../../include/trsm.h"
@@ -140,8 +142,8 @@ int solve_batched(int dtype, int layout, int64_t m, int64_t n, const unsigned ch
     bool owned = false;
     if (mem == nullptr || ws_bytes < total) {
         if (!may_alloc) return TRSM_ERR_WORKSPACE;
-        const cudaError_t e = cudaMallocAsync(&mem, total, st);
-        if (e != cudaSuccess) return cuda_status(e);
+        const int ae = workspace_alloc(&mem, total, st);
+        if (ae) return ae;
         owned = true;
     }
     int rc = TRSM_SUCCESS;
@@ -179,6 +181,43 @@ int solve_batched(int dtype, int layout, int64_t m, int64_t n, const unsigned ch
 }  // namespace
 
 namespace trsm {
+
+// Workspace the entry points allocate themselves comes from one stream-
+// ordered pool per device that keeps its memory between calls (release
+// threshold: never): mapping fresh pages for every call's workspace cost up
+// to a few hundred microseconds a call.  The pool holds at most the largest
+// workspace in use at once; trsm_llnn_ex and trsm_llnn_noalloc take nothing
+// from it.  Without a pool (creation failed) the device's current pool.
+int workspace_alloc(void **p, size_t bytes, cudaStream_t st) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDev] = {};
+    static bool tried[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaMemPool_t pool = nullptr;
+    if (dev >= 0 && dev < kMaxDev) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!tried[dev]) {
+            tried[dev] = true;
+            cudaMemPoolProps props{};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&pools[dev], &props) == cudaSuccess) {
+                uint64_t keep = UINT64_MAX;
+                cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+            } else {
+                pools[dev] = nullptr;
+                (void)cudaGetLastError();
+            }
+        }
+        pool = pools[dev];
+    }
+    e = pool ? cudaMallocFromPoolAsync(p, bytes, pool, st) : cudaMallocAsync(p, bytes, st);
+    return e == cudaSuccess ? TRSM_SUCCESS : cuda_status(e);
+}
 
 // Everything after validation.  ws: caller workspace or NULL (then it is
 // allocated stream-ordered when the blocked path needs one, unless
@@ -258,8 +297,8 @@ int solve_dispatch(int dtype, int layout, int64_t m, int64_t n, const void *alph
     bool owned = false;
     if (mem == nullptr || ws_bytes < total) {
         if (!may_alloc) return TRSM_ERR_WORKSPACE;
-        const cudaError_t e = cudaMallocAsync(&mem, total, st);
-        if (e != cudaSuccess) return cuda_status(e);
+        const int ae = workspace_alloc(&mem, total, st);
+        if (ae) return ae;
         owned = true;
     }
     int rc = TRSM_SUCCESS;
@@ -315,17 +354,24 @@ int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void 
     }
 }
 
-// Ainv <- I (m x m, column-major, ld): one thread per element of a column.
+// Ainv <- I (m x m, column-major, ld): CTA (x, y) writes rows x*1024 ..
+// x*1024 + 1023 of columns y, y + gridDim.y, ...; a thread four rows, 256
+// apart (coalesced stores, a few thousand CTAs in all).
 template <typename T>
-__global__ void set_identity_kernel(T *__restrict__ D, int64_t m, int64_t ld) {
-    const int64_t j = blockIdx.y;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < m; i += (int64_t)gridDim.x * blockDim.x) {
-        D[j * ld + i] = (i == j) ? one_of<T>() : zero_of<T>();
+__global__ void __launch_bounds__(256) set_identity_kernel(T *__restrict__ D, int64_t m, int64_t ld) {
+    const int64_t i0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+    for (int64_t j = blockIdx.y; j < m; j += gridDim.y) {
+        T *col = D + j * ld;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t i = i0 + 256 * k;
+            if (i < m) col[i] = (i == j) ? one_of<T>() : zero_of<T>();
+        }
     }
 }
 
 int launch_set_identity(int dtype, void *D, int64_t m, int64_t ld, cudaStream_t st) {
-    const dim3 grid((unsigned)((m + 255) / 256 < 64 ? (m + 255) / 256 : 64), (unsigned)m);
+    const dim3 grid((unsigned)((m + 1023) / 1024), (unsigned)(m < 512 ? m : 512));
     switch (dtype) {
         case TRSM_F32: set_identity_kernel<float><<<grid, 256, 0, st>>>(static_cast<float *>(D), m, ld); break;
         case TRSM_F64: set_identity_kernel<double><<<grid, 256, 0, st>>>(static_cast<double *>(D), m, ld); break;

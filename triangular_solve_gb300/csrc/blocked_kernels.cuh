@@ -267,12 +267,17 @@ __device__ __forceinline__ void inv_part_product(const T *A, int la, const T *Bm
         for (int y = 0; y < PC; ++y) Cm[(j0 + y) * lc + i0 + x] = acc[x][y];
 }
 
+// CTA b inverts rows and columns b*128 .. of L.  With diagonal blocks of
+// nbw = 128, 256 or 512 rows in W (ld nbw, one nbw^2 block after another),
+// its inverse lands at sub-block (q, q) of W_t, t = b / (nbw/128),
+// q = b % (nbw/128), and the rows above it in its columns are zeroed; the
+// blocks below the 128-row diagonal come from invert_blocks_doubling.
 // fill (optional): fill_words 32-bit words per CTA set to all ones, at
 // fill + blockIdx.x fill_words (the few-right-hand-side path's published copy
 // of X, cleared here instead of by a separate memset).
 template <typename T>
 __global__ void __launch_bounds__(256) inv_block128_kernel(const T *__restrict__ L, int64_t lda, int64_t m,
-                                                           T *__restrict__ W, uint32_t *__restrict__ fill,
+                                                           T *__restrict__ W, int nbw, uint32_t *__restrict__ fill,
                                                            int64_t fill_words) {
     extern __shared__ __align__(16) unsigned char inv_smem[];
     T *S = reinterpret_cast<T *>(inv_smem);  // D_t, then W_t: element (i, j) at j kInvLd + i
@@ -333,8 +338,13 @@ __global__ void __launch_bounds__(256) inv_block128_kernel(const T *__restrict__
         inv_part_product<T, 64, 4, 4, true, false, true>(Bi, kInvLd, Tmp, kInvTmpLd, C, kInvLd, tid);
         __syncthreads();
     }
-    T *Wt = W + (int64_t)blockIdx.x * kInvN * kInvN;
-    for (int e = tid; e < kInvN * kInvN; e += 256) Wt[e] = S[(e / kInvN) * kInvLd + e % kInvN];
+    const int per = nbw / kInvN, q = (int)(blockIdx.x % per);
+    T *Wt = W + (int64_t)(blockIdx.x / per) * nbw * nbw + (int64_t)q * kInvN * (nbw + 1);
+    for (int e = tid; e < kInvN * kInvN; e += 256) Wt[(e / kInvN) * nbw + e % kInvN] = S[(e / kInvN) * kInvLd + e % kInvN];
+    for (int e = tid; e < q * kInvN * kInvN; e += 256) {
+        const int i = e % (q * kInvN), j = e / (q * kInvN);
+        Wt[(int64_t)j * nbw + i - q * kInvN] = zero_of<T>();
+    }
     if (fill)
         for (int64_t e = tid; e < fill_words; e += 256) fill[(int64_t)blockIdx.x * fill_words + e] = 0xffffffffu;
 }

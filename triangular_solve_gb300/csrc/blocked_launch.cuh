@@ -1,6 +1,7 @@
 // Host driver of the blocked path for one element type.
 #pragma once
 
+#include <algorithm>
 #include <type_traits>
 
 #include "blocked_kernels.cuh"
@@ -157,6 +158,65 @@ static int invert_diagonal_blocks(const T *L, int64_t lda, int64_t m, int nb, T 
     return launch_status();
 }
 
+// f32 and c64: the diagonal blocks of nb = 128, 256 or 512 rows inverted
+// level by level.  Every 128-row diagonal block in one CTA
+// (inv_block128_kernel), then for s = 128, 256 .. nb/2 the lower-left block
+// of every 2s-row diagonal block [[A, 0], [C, D]] -- -D^{-1} (C A^{-1}), the
+// same formula as inside the kernel -- by two batched GEMMs, the middle
+// product in tmp (at least ceil(m/nb) (nb/2)^2 elements).  The diagonal
+// block whose rows run past m (the last one) has its GEMMs cut to its valid
+// rows, or its lower-left block zeroed when none are.
+template <typename T>
+static int invert_blocks_doubling(const T *L, int64_t lda, int64_t m, int nb, T *W, T *tmp, cudaStream_t st) {
+    const int64_t tb = (m + nb - 1) / nb;
+    constexpr size_t ismem = inv_block128_smem<T>();
+    int rc = cuda_status(
+        cudaFuncSetAttribute(inv_block128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ismem));
+    if (rc) return rc;
+    inv_block128_kernel<T><<<(unsigned)(tb * (nb / kInvN)), 256, ismem, st>>>(L, lda, m, W, nb, nullptr, 0);
+    if ((rc = launch_status())) return rc;
+    T one, minus_one;
+    memset(&one, 0, sizeof(T));
+    reinterpret_cast<typename Elem<T>::Real *>(&one)[0] = 1;
+    minus_one = one;
+    reinterpret_cast<typename Elem<T>::Real *>(&minus_one)[0] = -1;
+    const int64_t sW = (int64_t)nb * nb, sL = (int64_t)nb * (lda + 1);
+    for (int s = kInvN; s < nb && !rc; s *= 2) {
+        for (int o = 0; o < nb && !rc; o += 2 * s) {
+            // blocks t < full have all 2s rows inside the matrix
+            const int64_t full = m >= o + 2 * s ? std::min<int64_t>(tb, (m - o - 2 * s) / nb + 1) : 0;
+            auto run = [&](int64_t t, int64_t count, int64_t rows) {
+                // C A^{-1} into tmp (rows x s), then -D^{-1} (C A^{-1}) into W_t
+                GemmArgs<T> g1{};
+                g1.M = rows, g1.N = s, g1.K = s;
+                g1.A = L + (t * nb + o) * (lda + 1) + s, g1.lda = lda, g1.sA = sL;
+                g1.B = W + t * sW + (int64_t)o * (nb + 1), g1.ldb = nb, g1.sB = sW;
+                g1.C = tmp, g1.ldc = s, g1.sC = (int64_t)s * s;
+                g1.gamma = one, g1.beta = one, g1.beta_zero = 1;
+                int r = gemm_launch<T>(g1, st, (int)count);
+                if (r) return r;
+                GemmArgs<T> g2{};
+                g2.M = s, g2.N = s, g2.K = rows;
+                g2.A = W + t * sW + (int64_t)(o + s) * (nb + 1), g2.lda = nb, g2.sA = sW, g2.a_lower = 1;
+                g2.B = tmp, g2.ldb = s, g2.sB = (int64_t)s * s;
+                g2.C = W + t * sW + (int64_t)o * nb + o + s, g2.ldc = nb, g2.sC = sW;
+                g2.gamma = minus_one, g2.beta = one, g2.beta_zero = 1;
+                return gemm_launch<T>(g2, st, (int)count);
+            };
+            if (full > 0) rc = run(0, full, s);
+            if (!rc && full < tb) {
+                const int64_t t = tb - 1, rows = m - (t * nb + o + s);
+                if (rows > 0)
+                    rc = run(t, 1, rows);
+                else
+                    rc = cuda_status(cudaMemset2DAsync(W + t * sW + (int64_t)o * nb + o + s, nb * sizeof(T), 0,
+                                                       s * sizeof(T), s, st));
+            }
+        }
+    }
+    return rc;
+}
+
 // The few-right-hand-sides path (few_rhs.cuh): n <= kFewMaxN columns of a
 // column-major system of order m > kFewMinM, 16-byte aligned L columns, and
 // its data (few_rhs_bytes, which blocked_workspace_bytes covers) within the
@@ -213,7 +273,7 @@ static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, in
                                               (int)ismem));
         if (!rc) {
             inv_block128_kernel<T><<<(unsigned)tb, 256, ismem, st>>>(
-                L, lda, m, W, reinterpret_cast<uint32_t *>(xpub), n * NB * (int64_t)sizeof(T) / 4);
+                L, lda, m, W, (int)NB, reinterpret_cast<uint32_t *>(xpub), n * NB * (int64_t)sizeof(T) / 4);
             rc = launch_status();
         }
     } else {
@@ -321,11 +381,16 @@ int blocked_solve_typed(const BlockedArgs &a, cudaStream_t st) {
 
     // Phase 0: invert every diagonal block D_t (independent, one CTA each).
     timer.begin();
-    switch (nb) {
-        case 128: rc = invert_diagonal_blocks<T, 16>(L, a.lda, m, (int)nb, W, st); break;
-        case 256: rc = invert_diagonal_blocks<T, 32>(L, a.lda, m, (int)nb, W, st); break;
-        case 512: rc = invert_diagonal_blocks<T, 64>(L, a.lda, m, (int)nb, W, st); break;
-        default: return -9;
+    if (nb != 128 && nb != 256 && nb != 512) return -9;
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value) {
+        // the middle products live in the tensor-core panels, unused until the solve
+        rc = invert_blocks_doubling<T>(L, a.lda, m, (int)nb, W, static_cast<T *>(tc_panels), st);
+    } else {
+        switch (nb) {
+            case 128: rc = invert_diagonal_blocks<T, 16>(L, a.lda, m, (int)nb, W, st); break;
+            case 256: rc = invert_diagonal_blocks<T, 32>(L, a.lda, m, (int)nb, W, st); break;
+            default: rc = invert_diagonal_blocks<T, 64>(L, a.lda, m, (int)nb, W, st); break;
+        }
     }
     if (rc || (rc = timer.end(0))) return rc;
 

@@ -187,6 +187,9 @@ int solve_dispatch(int dtype, int layout, int64_t m, int64_t n, const void *alph
 // Row-major <-> column-major copy of a rows x cols matrix (out-of-place),
 // used to run row-major inputs through the column-major blocked path.
 // With nz > 1: nz such copies, src and dst advancing by s_src / s_dst elements.
+// Workspace of the entry points that allocate their own: the library's
+// per-device stream-ordered pool (api.cu); freed with cudaFreeAsync.
+int workspace_alloc(void **p, size_t bytes, cudaStream_t st);
 int launch_transpose_copy(int elem_bytes, const void *src, int64_t ld_src, void *dst, int64_t ld_dst,
                           int64_t rows, int64_t cols, cudaStream_t st, int64_t s_src = 0, int64_t s_dst = 0,
                           int nz = 1);

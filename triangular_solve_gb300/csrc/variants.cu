@@ -95,8 +95,9 @@ int variant_solve(trsm_dtype_t dtype, bool right, bool trans, bool rev, bool con
     const size_t a_bytes = round256(k * k * (int64_t)sizeof(T));
     const size_t b_bytes = right ? (size_t)round256(n * m * (int64_t)sizeof(T)) : 0;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, a_bytes + b_bytes, st);
-    if (e != cudaSuccess) return cuda_status(e);
+    const int ae = workspace_alloc(&ws, a_bytes + b_bytes, st);
+    if (ae) return ae;
+    cudaError_t e = cudaSuccess;
     void *Ap = ws;
     void *Bp = right ? static_cast<char *>(ws) + a_bytes : B;
     const int64_t ldp = right ? n : ldb;
