@@ -230,3 +230,27 @@ def test_persistent_c64_strided_layouts(env, m, geom):
         kw = dict(lda=m + 2, ldb=m + 4) if geom == "padded" else dict(stride_a=m * m + 32, stride_b=m * n + 16)
         _parity(env, "c64", L, B, 1.0, f"{geom} m={m}", **kw)
     assert env["tg"].trsm_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("m,n,batch,layout", [
+    (8, 8, 16384, "col"),     # the sweep's m = 8 point
+    (8, 3, 4096, "row"),      # reciprocals shared from three columns on
+    (7, 37, 300, "col"),      # ragged m, odd n: systems straddle CTAs
+    (3, 1, 1000, "row"),      # reciprocals per thread
+    (5, 2, 3, "col"),
+    (1, 300, 2, "row"),
+])
+def test_tiny_systems(env, dtype, m, n, batch, layout):
+    """m <= 8 runs one thread per (system, column): batches up to the
+    sweep's 16384, both layouts, padded leading dimensions and gaps between
+    systems, complex alpha."""
+    L, B = ti.generate(dtype, m, n, batch, kind="dd64", seed=m * 100 + n)
+    alpha = (0.75 - 0.5j) if ti.IS_COMPLEX[dtype] else 0.75
+    ld_b = (m if layout == "col" else n) + 3
+    a, b, geo = storage_pair(L, B, layout=layout, lda=m + 1, ldb=ld_b,
+                             stride_a=m * (m + 1) + 8, stride_b=ld_b * (n if layout == "col" else m) + 16)
+    raw = gpu_solve_buffers(dtype, a, b, geo, alpha, env["torch"], env["tg"])
+    ref = oracle_buffers(dtype, a, b, geo, alpha, env["oracle"])
+    assert_padding_untouched(raw, b, geo)
+    assert_parity(dtype, logical(raw, geo), logical(ref, geo), f"tiny {dtype} m={m} n={n} {layout}")

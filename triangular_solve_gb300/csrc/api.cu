@@ -64,6 +64,14 @@ int nearest_nb(int dtype, int64_t m) {
 constexpr int kFastNotApplicableCode = -100000;  // launch_fast_*: preconditions not met
 
 int launch_small(int dtype, const SmallArgs &a, cudaStream_t st) {
+    if (a.m <= 8 && a.batch * a.n <= (int64_t)256 * 0x7fffffff) {
+        switch (dtype) {
+            case TRSM_F32: return launch_tiny_f32(a, st);
+            case TRSM_F64: return launch_tiny_f64(a, st);
+            case TRSM_C64: return launch_tiny_c64(a, st);
+            default: return launch_tiny_c128(a, st);
+        }
+    }
     if (a.n <= 8) {
         switch (dtype) {
             case TRSM_F32: return launch_rowlane_f32(a, st);

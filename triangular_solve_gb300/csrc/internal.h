@@ -32,6 +32,11 @@ int launch_rowlane_f32(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_f64(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_c64(const SmallArgs &a, cudaStream_t st);
 int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st);
+// m <= 8: one thread per (system, right-hand-side column).
+int launch_tiny_f32(const SmallArgs &a, cudaStream_t st);
+int launch_tiny_f64(const SmallArgs &a, cudaStream_t st);
+int launch_tiny_c64(const SmallArgs &a, cudaStream_t st);
+int launch_tiny_c128(const SmallArgs &a, cudaStream_t st);
 
 // Fast path of the thread-per-column kernel for aligned full-size systems
 // (m in {8, 16, 32, 48, 64}, and 128 for batches of medium systems); returns

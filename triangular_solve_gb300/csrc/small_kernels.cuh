@@ -38,6 +38,59 @@ struct SmallGeom {
     int w;    // RHS columns per CTA slice (colreg) / register columns (rowlane)
 };
 
+// Systems of order m <= 8: one thread per (system, right-hand-side
+// column), the column in registers, the triangle read through L1 (a warp's
+// threads share a few systems, so most reads are broadcasts), forward
+// substitution with the diagonal's reciprocals -- computed once per system
+// into shared memory when three or more columns share it (in FP64 the
+// reciprocals were most of the work).  Either layout.  At this size a warp
+// per system or a CTA per few systems leaves most lanes idle; here every
+// thread does a whole column, and the grid is batch x n threads.
+constexpr int kTinyM = 8;
+template <typename T>
+__global__ void __launch_bounds__(256) small_tiny_kernel(const SmallGeom g, const T alpha) {
+    constexpr int M = kTinyM, kMaxSys = 256 / 3 + 2;  // systems a CTA touches when n >= 3
+    __shared__ T rinv[kMaxSys * M];
+    const int64_t total = g.batch * g.n, gid0 = (int64_t)blockIdx.x * 256, gid = gid0 + threadIdx.x;
+    const int m = g.m;
+    const T *A0 = static_cast<const T *>(g.A);
+    // element (i, k): column-major i + k ld, row-major i ld + k
+    const int64_t ar = g.layout ? g.lda : 1, ac = g.layout ? 1 : g.lda;
+    const int64_t br = g.layout ? g.ldb : 1, bc = g.layout ? 1 : g.ldb;
+    const bool shared_rinv = g.n >= 3;
+    const int64_t b0 = gid0 / g.n;
+    if (shared_rinv) {
+        const int64_t last = (gid0 + 255 < total ? gid0 + 255 : total - 1);
+        const int nsys = (int)(last / g.n - b0 + 1);
+        for (int e = threadIdx.x; e < nsys * M; e += 256) {
+            const int k = e % M;
+            rinv[e] = k < m ? recip(ldg(A0 + (b0 + e / M) * g.sA + k * (ar + ac))) : zero_of<T>();
+        }
+        __syncthreads();
+    }
+    if (gid >= total) return;
+    const int64_t b = gid / g.n;
+    const int j = (int)(gid - b * g.n);
+    const T *A = A0 + b * g.sA;
+    T *B = static_cast<T *>(g.B) + b * g.sB;
+    T x[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) x[i] = i < m ? mul(alpha, B[i * br + j * bc]) : zero_of<T>();
+#pragma unroll
+    for (int k = 0; k < M; ++k) {
+        if (k < m) {
+            const T d = shared_rinv ? rinv[(b - b0) * M + k] : recip(ldg(A + k * (ar + ac)));
+            x[k] = mul(x[k], d);
+#pragma unroll
+            for (int i = k + 1; i < M; ++i)
+                if (i < m) x[i] = fms(ldg(A + i * ar + k * ac), x[k], x[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (i < m) B[i * br + j * bc] = x[i];
+}
+
 // Vector width (elements per 16-byte shared load).
 template <typename T> struct Vec { static constexpr int kN = sizeof(T) >= 16 ? 1 : 16 / (int)sizeof(T); };
 

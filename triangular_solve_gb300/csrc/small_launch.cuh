@@ -105,6 +105,17 @@ inline SmallGeom small_geom(const SmallArgs &a) {
     return g;
 }
 
+// m <= 8: a thread per (system, column).
+template <typename T>
+int launch_tiny_typed(const SmallArgs &a, cudaStream_t st) {
+    const SmallGeom g = small_geom(a);
+    T alpha;
+    memcpy(&alpha, a.alpha, sizeof(T));
+    const int64_t threads = g.batch * g.n;
+    small_tiny_kernel<T><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(g, alpha);
+    return launch_status();
+}
+
 // Thread-per-column kernel (n > 8).
 template <typename T>
 int launch_colreg_typed(const SmallArgs &a, cudaStream_t st) {

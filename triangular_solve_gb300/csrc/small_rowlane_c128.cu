@@ -3,4 +3,5 @@
 
 namespace trsm {
 int launch_rowlane_c128(const SmallArgs &a, cudaStream_t st) { return launch_rowlane_typed<double2>(a, st); }
+int launch_tiny_c128(const SmallArgs &a, cudaStream_t st) { return launch_tiny_typed<double2>(a, st); }
 }  // namespace trsm
