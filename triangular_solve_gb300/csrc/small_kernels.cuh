@@ -114,8 +114,9 @@ struct Packed {
 };
 
 // Shared-memory image of one system:
-//   Ls   packed strictly-lower columns of L (see Packed); rows at or above
-//        the diagonal and padding rows >= m hold zero.
+//   Ls   packed strictly-lower columns of L (see Packed); padding rows
+//        >= m hold zero; the never-read rows s(k)..k of column k hold zero
+//        or, when whole 16-byte groups are copied, the matrix's own values.
 //   dinv M reciprocals of the diagonal (zero for padding rows >= m).
 //   Bs   w columns of the RHS, column stride M + 1 (odd, so a thread per
 //        column reads its own column without bank conflicts).
@@ -142,12 +143,24 @@ __device__ __forceinline__ void stage_system(const SmallGeom &g, T *Ls, T *dinv,
     const T z = zero_of<T>();
     using P = Packed<T, M>;
     if (g.layout == 0) {
-        for (int e = tid; e < M * M; e += nthr) {
-            const int k = e / M, i = e - k * M;
-            if (i < P::s(k)) continue;
-            T *d = Ls + P::off(k) + (i - P::s(k));
-            if (i > k && i < m) cp_async<sizeof(T)>(d, A + (int64_t)k * g.lda + i);
-            else *d = z;
+        constexpr int V = P::V, G = M / V;  // elements per 16 bytes, 16-byte groups per full column
+        if (V > 1 && m == M && (reinterpret_cast<uintptr_t>(A) & 15) == 0 && g.lda % V == 0) {
+            // full-size, aligned: whole 16-byte groups of column k from row
+            // s(k) (its rows s(k)..k come along and are never read), a
+            // fraction of the element-wise loop's instructions
+            for (int e = tid; e < M * G; e += nthr) {
+                const int k = e / G, q = e - k * G;
+                if (q * V < P::s(k)) continue;
+                cp_async<16>(Ls + P::off(k) + (q * V - P::s(k)), A + (int64_t)k * g.lda + q * V);
+            }
+        } else {
+            for (int e = tid; e < M * M; e += nthr) {
+                const int k = e / M, i = e - k * M;
+                if (i < P::s(k)) continue;
+                T *d = Ls + P::off(k) + (i - P::s(k));
+                if (i > k && i < m) cp_async<sizeof(T)>(d, A + (int64_t)k * g.lda + i);
+                else *d = z;
+            }
         }
         for (int e = tid; e < wcols * M; e += nthr) {
             const int c = e / M, i = e - c * M;
