@@ -188,14 +188,29 @@ def test_narrow_path_large(env, dtype):
     assert_parity(dtype, xg, xr, f"narrow {dtype} m={m}")
 
 
+@pytest.mark.parametrize("dtype,n", [("f32", 3), ("c64", 1)])
+def test_few_rhs_more_block_rows_than_ctas(env, dtype, n):
+    """m = 18688: 146 block rows, more than the resident clusters of four
+    hold (one CTA per SM), so some CTAs take a second block row and the
+    hand-over between neighbours spans passes."""
+    m = 18688
+    L, B = ti.generate(dtype, m, n, 1, kind="ddm", seed=5)
+    alpha = (0.25 - 1.0j) if ti.IS_COMPLEX[dtype] else 0.75
+    xg, xr = _ex_solve(env, dtype, L, B, alpha, 0)
+    assert env["tg"].trsm_device_status() == 0
+    assert_parity(dtype, xg, xr, f"few-rhs multi-pass {dtype} m={m} n={n}")
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("m,n", [(513, 1), (640, 8), (1000, 2), (2049, 5), (4096, 3)])
 def test_few_rhs_persistent_path(env, dtype, m, n):
     """n <= 8 with 16-byte aligned columns of L: the persistent few-right-hand-
     side kernel (one CTA per 128-row block row, each publishing its x_t to
-    the CTAs below), ragged last block rows, complex alpha, padded leading
+    the CTAs below; for f32 with n > 1 and for c64 in clusters of four whose
+    CTAs hand x_t to the next one directly), ragged last block rows (idle
+    CTAs in the last cluster), complex alpha, padded leading
     dimensions; the device status word stays clear, and the phase times show
-    that this kernel ran (no separate applies; complex128 from three columns
+    that this kernel ran (no separate applies; complex128 from five columns
     on takes the blocked path)."""
     torch, tg = env["torch"], env["tg"]
     per16 = {"f32": 4, "f64": 2, "c64": 2, "c128": 1}[dtype]  # elements in 16 bytes
@@ -211,7 +226,7 @@ def test_few_rhs_persistent_path(env, dtype, m, n):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     tA, tB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     ms = tg.trsm_llnn_profile(dtype, m, n, alpha, tA, geo["lda"], tB, geo["ldb"], 0, ws, ws_bytes)
-    if dtype == "c128" and n > 2:   # complex128 keeps three or more columns on the blocked path
+    if dtype == "c128" and n > 4:   # complex128 keeps five or more columns on the blocked path
         assert ms[1] > 0.0, f"blocked {dtype} m={m} n={n}: phases {ms}"
     else:
         assert ms[1] == 0.0 and ms[2] > 0.0, f"few-rhs {dtype} m={m} n={n}: phases {ms}"

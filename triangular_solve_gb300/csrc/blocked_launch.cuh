@@ -223,25 +223,82 @@ static int invert_blocks_doubling(const T *L, int64_t lda, int64_t m, int nb, T 
 // workspace of ws_bytes.
 constexpr int64_t kFewMinM = 512;
 
-// complex128 only up to two columns: from three on, each block row's FP64
+// complex128 only up to four columns: from five on, each block row's FP64
 // work on the chain (one SM) outweighs what the kernel saves, and the
-// blocked path is as fast or faster.
+// blocked path is faster (m = 16384, n = 8: 37 against 30 ms; n = 3: 19
+// against 30 ms).
 template <typename T>
 static bool few_rhs_usable(int64_t m, int64_t n, const T *L, int64_t lda, size_t ws_bytes) {
-    const int64_t max_n = std::is_same<T, double2>::value ? 2 : kFewMaxN;
+    const int64_t max_n = std::is_same<T, double2>::value ? 4 : kFewMaxN;
     return n >= 1 && n <= max_n && m > kFewMinM && ((reinterpret_cast<uintptr_t>(L) & 15) == 0) &&
            (lda * (int64_t)sizeof(T)) % 16 == 0 && few_rhs_bytes((int)sizeof(T), m, n) <= ws_bytes;
 }
 
+// The persistent kernel with the right-hand-side count compiled in.  CL:
+// clusters of four (else two) consecutive block rows, which hand x_t to the
+// next one in shared memory -- the grid a multiple of the cluster, every
+// cluster resident (a cooperative launch); kFewNoCluster when neither size
+// can be placed.  Without CL a plain cooperative launch.
+constexpr int kFewNoCluster = -300000;
+template <typename T, bool CL>
+static int few_rhs_launch(int64_t n, int64_t tb, void **args, cudaStream_t st) {
+    constexpr size_t smem = few_rhs_smem<T, CL>();
+    auto kern = n <= 1   ? few_rhs_kernel<T, 1, CL>
+                : n <= 2 ? few_rhs_kernel<T, 2, CL>
+                : n <= 4 ? few_rhs_kernel<T, 4, CL>
+                         : few_rhs_kernel<T, 8, CL>;
+    int rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    if (rc) return rc;
+    if constexpr (CL) {
+        for (int K : {4, 2}) {
+            cudaLaunchAttribute at[2];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)K;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            at[1].id = cudaLaunchAttributeCooperative;
+            at[1].val.cooperative = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)K);
+            cfg.blockDim = dim3(320);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+                (void)cudaGetLastError();
+                continue;
+            }
+            const int64_t want = (tb + K - 1) / K;
+            cfg.gridDim = dim3((unsigned)((want < clusters ? want : clusters) * K));
+            cfg.numAttrs = 2;
+            if (cudaLaunchKernelExC(&cfg, (const void *)kern, args) == cudaSuccess) return TRSM_SUCCESS;
+            (void)cudaGetLastError();  // e.g. too many blocks for a cooperative launch: the next size
+        }
+        return kFewNoCluster;
+    } else {
+        int dev = 0, sms = 0, per_sm = 0;
+        rc = cuda_status(cudaGetDevice(&dev));
+        if (!rc) rc = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        if (!rc) rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 320, smem));
+        if (!rc && per_sm < 1) rc = TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidConfiguration;
+        if (rc) return rc;
+        const int64_t cap = (int64_t)sms * per_sm;
+        const unsigned grid = (unsigned)(tb < cap ? tb : cap);
+        return cuda_status(cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(320), args, smem, st));
+    }
+}
+
 // The inversion of the diagonal blocks (few_nb<T>() rows), then the
-// persistent kernel (a cooperative launch: its CTAs wait on one another's
-// published results, so all of them must be resident at once).  L and the inverted
+// persistent kernel (a cooperative launch in clusters: its CTAs wait on one
+// another's results, so all of them must be resident at once).  L and the inverted
 // blocks are read by TMA tensor copies: float views, a column's block of
 // rows as boxes of at most 256 floats.
 template <typename T>
 static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, int64_t ldb, T alpha, void *ws,
                          cudaStream_t st, float *inv_ms, float *solve_ms) {
-    using Cfg = FewCfg<T>;
+    using Cfg = FewCfg<T, false>;  // the geometry (NB, Q, BR, KC) is the same in both forms
     constexpr int64_t NB = Cfg::NB;
     const int64_t tb = (m + NB - 1) / NB;
     T *W = static_cast<T *>(ws);
@@ -283,23 +340,19 @@ static int few_rhs_solve(const T *L, int64_t lda, int64_t m, int64_t n, T *B, in
     int *status = nullptr;
     if (!rc) rc = device_status_word(&status);
     if (inv_ms) cudaEventRecord(e[1], st);
-    constexpr size_t smem = few_rhs_smem<T>();
-    auto kern = n <= 1 ? few_rhs_kernel<T, 1> : n <= 2 ? few_rhs_kernel<T, 2> : n <= 4 ? few_rhs_kernel<T, 4>
-                                                                                       : few_rhs_kernel<T, 8>;
-    if (!rc) rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    int dev = 0, sms = 0, per_sm = 0;
-    if (!rc) rc = cuda_status(cudaGetDevice(&dev));
-    if (!rc) rc = cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    if (!rc) rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 320, smem));
-    if (!rc && per_sm < 1) rc = TRSM_ERR_CUDA_BASE + (int)cudaErrorInvalidConfiguration;
     if (!rc) {
-        const int64_t cap = (int64_t)sms * per_sm;
-        const unsigned grid = (unsigned)(tb < cap ? tb : cap);
         const int ni = (int)n;
         const int64_t limit = int64_t(1) << 22;  // polls of a published block row (each a round trip to L2)
         void *args[] = {(void *)&mapL, (void *)&mapW, (void *)&m, (void *)&ni, (void *)&B, (void *)&ldb,
                         (void *)&alpha, (void *)&xpub, (void *)&status, (void *)&limit};
-        rc = cuda_status(cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(320), args, smem, st));
+        // The cluster form for f32 with two or more columns and for complex64
+        // (measured faster there); not for one f32 column (0.24 ms without
+        // against 0.26 ms with, m = 16384) nor for the FP64 types, whose chain
+        // is bound by one SM's FP64 rate.
+        rc = kFewNoCluster;
+        if constexpr (std::is_same<T, float>::value || std::is_same<T, float2>::value)
+            if (std::is_same<T, float2>::value || n > 1) rc = few_rhs_launch<T, true>(n, tb, args, st);
+        if (rc == kFewNoCluster) rc = few_rhs_launch<T, false>(n, tb, args, st);
     }
     if (inv_ms) {
         cudaEventRecord(e[2], st);

@@ -47,7 +47,9 @@ constexpr int few_nb() {
     return (int)kFewNb;
 }
 
-template <typename T>
+// CL: the cluster form (x_{t-1} handed over in shared memory, see the
+// kernel), which needs one more slot.
+template <typename T, bool CL>
 struct FewCfg {
     static constexpr int NB = few_nb<T>();
     static constexpr int HALVES = 256 / NB;                         // consumer threads per row
@@ -57,8 +59,8 @@ struct FewCfg {
     static constexpr int KPT = NB / KC;                             // chunks per tile
     static constexpr int kChunk = NB * KC;                          // elements per chunk
     static constexpr int XS = sizeof(T) >= 16 ? 2 : 4;              // x slots
-    static constexpr int kSlot = NB * kFewMaxN;                     // elements per x slot (and rbuf, part)
-    static constexpr size_t kFixed = (size_t)(XS + 2) * kSlot * sizeof(T);
+    static constexpr int kSlot = NB * kFewMaxN;                     // elements per x slot (and rbuf, part, dsx)
+    static constexpr size_t kFixed = (size_t)(XS + 2 + (CL ? 1 : 0)) * kSlot * sizeof(T);
     static constexpr int ST = (int)((220 * 1024 - kFixed) / (kChunk * sizeof(T)));  // ring stages
     static constexpr size_t kSmem = (size_t)ST * kChunk * sizeof(T) + kFixed + 1024;
     static_assert(KC * NB * (int)sizeof(T) == 32768 && KPT >= 2 && KC % (2 * HALVES) == 0, "32 KB chunks");
@@ -122,6 +124,42 @@ __device__ __forceinline__ void store_published(float2 *p, float2 v) {
 __device__ __forceinline__ void store_published(double2 *p, double2 v) {
     asm volatile("st.relaxed.gpu.global.v2.f64 [%0], {%1, %2};\n" ::"l"(p), "d"(v.x), "d"(v.y) : "memory");
 }
+// Every thread of every CTA of the cluster (a CTA of its own without one).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;\n" ::: "memory");
+}
+// v into the same shared-memory location of CTA `rank` of the cluster,
+// completing that CTA's mbarrier at bar's address by sizeof(v) bytes.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_async_remote(float *p, float v, uint64_t *bar, uint32_t rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(
+                     cluster_addr(p, rank)),
+                 "r"(__float_as_uint(v)), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_remote(double *p, double v, uint64_t *bar, uint32_t rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];\n" ::"r"(
+                     cluster_addr(p, rank)),
+                 "l"(__double_as_longlong(v)), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_remote(float2 *p, float2 v, uint64_t *bar, uint32_t rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];\n" ::"r"(
+                     cluster_addr(p, rank)),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_remote(double2 *p, double2 v, uint64_t *bar, uint32_t rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];\n" ::"r"(
+                     cluster_addr(p, rank)),
+                 "l"(__double_as_longlong(v.x)), "l"(__double_as_longlong(v.y)), "r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+
 // two consecutive elements of shared memory (8-byte aligned pairs of f32,
 // 16-byte of the others) in one access where the width allows
 __device__ __forceinline__ void load_pair(const float *p, float &a, float &b) {
@@ -143,11 +181,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;
 // launcher picks the smallest of 1, 2, 4, 8): a guarded loop over a fixed
 // eight would still issue the idle columns' FMAs, which on the FP64 pipe
 // cost as much as the real ones.
-template <typename T, int NC>
+template <typename T, int NC, bool CL>
 __global__ void __launch_bounds__(320, 1)
     few_rhs_kernel(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapW, int64_t m,
                    int n, T *B, int64_t ldb, const T alpha, T *xpub, int *status, const int64_t poll_limit) {
-    using C = FewCfg<T>;
+    using C = FewCfg<T, CL>;
     constexpr int NB = C::NB, KC = C::KC, KPT = C::KPT, ST = C::ST, XS = C::XS, BR = C::BR, Q = C::Q;
     // f32 with one right-hand side holds the tile on the chain and W_t in
     // registers (see the consumers); W_t then comes first in a block row's
@@ -155,16 +193,36 @@ __global__ void __launch_bounds__(320, 1)
     constexpr bool kReg = std::is_same<T, float>::value && NC == 1;
     constexpr int KH = KC / C::HALVES;  // columns of a chunk per thread
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full[ST], empty[ST], xfull[XS], xempty[XS];
+    __shared__ __align__(8) uint64_t full[ST], empty[ST], xfull[XS], xempty[XS], dsbar;
     __shared__ volatile int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     T *ring = reinterpret_cast<T *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));  // [ST][chunk]
     T *xs = ring + ST * C::kChunk;                                                  // [XS][8][NB]
     T *rbuf = xs + XS * C::kSlot;                                                   // [8][NB]: r_t
     T *part = rbuf + C::kSlot;                                                      // [8][NB]
+    T *dsx = part + C::kSlot;  // [8][NB]: x_{t-1}, written by the CTA before this one in the cluster
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t tb = (m + NB - 1) / NB;
+    // In a cluster of K CTAs (consecutive block rows, the grid a multiple of
+    // K), every CTA but the cluster's first receives x_{t-1} straight into
+    // its shared memory from the CTA that solves it (st.async, completing
+    // dsbar), and every CTA but the last sends x_t on: the hop through L2
+    // remains only at cluster boundaries and for the block rows further down.
+    // (kept in shared memory, read where needed: the f32 consumers' registers
+    // are full with L_{t,t-1} and W_t)
+    __shared__ int sh_rank, sh_left, sh_right;
+    if constexpr (CL)
+        for (int e = tid; e < C::kSlot; e += blockDim.x) dsx[e] = zero_of<T>();  // columns >= n stay zero
     if (tid == 0) {
+        if constexpr (CL) {
+            uint32_t crank, csize;
+            asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(crank));
+            asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(csize));
+            sh_rank = (int)crank;
+            sh_left = crank > 0;
+            sh_right = crank + 1 < csize;
+            mbar_init(smem_u32(&dsbar), 1);
+        }
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 8);
@@ -177,8 +235,10 @@ __global__ void __launch_bounds__(320, 1)
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncthreads();
+    // every CTA of the cluster has its barriers ready before any st.async
+    if constexpr (CL) cluster_sync_all();
 
-    if (warp == 0) {
+    auto copies = [&]() {
         // ---------------------------------------------------------- copies
         if (lane != 0) return;
         int64_t g = 0;  // chunks issued
@@ -214,17 +274,17 @@ __global__ void __launch_bounds__(320, 1)
             for (int64_t h = (g > ST ? g - ST : 0); h < g; ++h)
                 mbar_wait(smem_u32(&full[h % ST]), (uint32_t)((h / ST) & 1));
         }
-        return;
-    }
+    };
 
-    if (warp == 1) {
+    auto poller = [&]() {
         // ---------------------------------------------------------- x_s
         constexpr int kPollE = NB * NC / 32;                        // elements a lane polls
         constexpr bool kPollTwo = kPollE * sizeof(T) <= 64;         // two polls held in registers
         constexpr long long kPollGap = 600;                         // cycles, about half an L2 round trip
         int64_t gx = 0;
         for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
-            for (int64_t s = 0; s < t; ++s, ++gx) {
+            for (int64_t s = 0; s < t; ++s) {
+                if (CL && s == t - 1 && sh_left) continue;  // x_{t-1} arrives in dsx
                 const int slot = (int)(gx % XS);
                 bool ok = true;
                 if (gx >= XS) ok = mbar_wait(smem_u32(&xempty[slot]), (uint32_t)((gx / XS - 1) & 1));
@@ -296,11 +356,12 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&xfull[slot]));
+                ++gx;
             }
         }
-        return;
-    }
+    };
 
+    auto consume = [&]() {
     // -------------------------------------------------------------- consume
     // Every consumer warp runs the same sequence of stage releases and
     // consumer barriers whatever happens: after a failed wait (abort_flag set)
@@ -416,8 +477,16 @@ __global__ void __launch_bounds__(320, 1)
         }
     };
     T Lreg[HC], Wreg[HC];
-    for (int64_t t = blockIdx.x; t < tb; t += gridDim.x) {
+    // dsbar: one phase per block row (t >= 1 whenever there is a left neighbour), armed by
+    // thread ct 0 at the block row's start -- not after a failure, when the
+    // earlier phase may still be open (the end of the kernel drains them)
+    uint32_t pass = 0, armed = 0;
+    for (int64_t t = blockIdx.x; t < tb; t += gridDim.x, ++pass) {
         const int64_t r0 = t * NB;
+        if (CL && ct == 0 && sh_left && !abort_flag) {
+            mbar_expect_tx(smem_u32(&dsbar), (uint32_t)(n * NB * (int)sizeof(T)));
+            ++armed;
+        }
         // alpha b_t, loaded now: off the chain of block rows
         T ab[NC];
 #pragma unroll
@@ -428,17 +497,26 @@ __global__ void __launch_bounds__(320, 1)
         for (int cc = 0; cc < NC; ++cc) acc[cc] = zero_of<T>();
         const int64_t s_reg = kReg ? t - 1 : t;  // the tile from registers
         if (kReg) preload(Wreg);
-        for (int64_t s = 0; s < t; ++s, ++gx) {
+        for (int64_t s = 0; s < t; ++s) {
+            const bool local = CL && s == t - 1 && sh_left;  // x_s in dsx, not in a slot
             const int slot = (int)(gx % XS);
             if (s == s_reg) preload(Lreg);
-            if (!abort_flag && !mbar_wait(smem_u32(&xfull[slot]), (uint32_t)((gx / XS) & 1))) fail();
-            if (s == s_reg) {
-                if (!abort_flag) reg_matvec(Lreg, xs + slot * C::kSlot, acc);
-            } else {
-                for (int kc = 0; kc < KPT; ++kc) chunk(xs + slot * C::kSlot, kc * KC, acc);
+            if (local) {
+                if (!abort_flag && !mbar_wait(smem_u32(&dsbar), pass & 1u)) fail();
+            } else if (!abort_flag && !mbar_wait(smem_u32(&xfull[slot]), (uint32_t)((gx / XS) & 1))) {
+                fail();
             }
-            __syncwarp();
-            if (wl) mbar_arrive(smem_u32(&xempty[slot]));
+            const T *xsrc = local ? dsx : xs + slot * C::kSlot;
+            if (s == s_reg) {
+                if (!abort_flag) reg_matvec(Lreg, xsrc, acc);
+            } else {
+                for (int kc = 0; kc < KPT; ++kc) chunk(xsrc, kc * KC, acc);
+            }
+            if (!local) {
+                __syncwarp();
+                if (wl) mbar_arrive(smem_u32(&xempty[slot]));
+                ++gx;
+            }
         }
         // every tile is in: r_t = alpha b_t - sum_s L_ts x_s
         combine(acc);
@@ -460,21 +538,44 @@ __global__ void __launch_bounds__(320, 1)
         // X over b_t, and the published copy for the block rows below (also
         // after a failure -- the status word then says the result is void --
         // so that the CTAs waiting on it finish instead of timing out)
+        // (and to the next CTA of the cluster, which solves block row t + 1)
+        const bool send = CL && t + 1 < tb && sh_right;
         if (half == 0 && r0 + row < m) {
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc)
                 if (cc < n) {
                     B[cc * ldb + r0 + row] = acc[cc];
                     store_published(xpub + (t * n + cc) * NB + row, canon(acc[cc]));
+                    if (send) st_async_remote(dsx + cc * NB + row, acc[cc], &dsbar, (uint32_t)sh_rank + 1);
                 }
         }
         consumer_sync();  // rbuf and part are rewritten for the next block row
     }
+    // after a failure every hand-off the left neighbour sends (it sends one
+    // per block row whatever happens) must still land before this CTA may
+    // exit: wait for the open phase, then arm and wait for the rest in order
+    if (CL && ct == 0 && sh_left && armed < pass) {
+        if (armed > 0) mbar_wait(smem_u32(&dsbar), (armed - 1) & 1u);
+        for (uint32_t q = armed; q < pass; ++q) {
+            mbar_expect_tx(smem_u32(&dsbar), (uint32_t)(n * NB * (int)sizeof(T)));
+            mbar_wait(smem_u32(&dsbar), q & 1u);
+        }
+    }
+    };
+
+    if (warp == 0)
+        copies();
+    else if (warp == 1)
+        poller();
+    else
+        consume();
+    // no CTA leaves while a neighbour may still write into its shared memory
+    if constexpr (CL) cluster_sync_all();
 }
 
-template <typename T>
+template <typename T, bool CL>
 constexpr size_t few_rhs_smem() {
-    return FewCfg<T>::kSmem;
+    return FewCfg<T, CL>::kSmem;
 }
 
 }  // namespace trsm
