@@ -37,11 +37,6 @@ __device__ __forceinline__ void inv_l1_prefetch(T *slot, const T *L, int64_t lda
     else slot[tid] = zero_of<T>();
 }
 
-template <typename T> __device__ __forceinline__ T one_of();
-template <> __device__ __forceinline__ float one_of<float>() { return 1.f; }
-template <> __device__ __forceinline__ double one_of<double>() { return 1.0; }
-template <> __device__ __forceinline__ float2 one_of<float2>() { return make_float2(1.f, 0.f); }
-template <> __device__ __forceinline__ double2 one_of<double2>() { return make_double2(1.0, 0.0); }
 
 template <typename T, int IB, int K>
 struct InvL1Steps {

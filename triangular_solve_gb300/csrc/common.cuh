@@ -24,6 +24,11 @@ template <> __host__ __device__ __forceinline__ float zero_of<float>() { return 
 template <> __host__ __device__ __forceinline__ double zero_of<double>() { return 0.0; }
 template <> __host__ __device__ __forceinline__ float2 zero_of<float2>() { return make_float2(0.f, 0.f); }
 template <> __host__ __device__ __forceinline__ double2 zero_of<double2>() { return make_double2(0.0, 0.0); }
+template <typename T> __device__ __forceinline__ T one_of();
+template <> __device__ __forceinline__ float one_of<float>() { return 1.f; }
+template <> __device__ __forceinline__ double one_of<double>() { return 1.0; }
+template <> __device__ __forceinline__ float2 one_of<float2>() { return make_float2(1.f, 0.f); }
+template <> __device__ __forceinline__ double2 one_of<double2>() { return make_double2(1.0, 0.0); }
 
 // a * b
 __device__ __forceinline__ float mul(float a, float b) { return a * b; }
