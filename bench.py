@@ -53,7 +53,7 @@ SQUARE_KERNEL = {"f32": "small_tma_f32_kernel<64, 2>", "f64": "small_fast_kernel
                  "c64": "small_fast_kernel<float2, 64, 64, 1, 16, 2>",
                  "c128": "small_fast_kernel<double2, 64, 64, 1, 16, 1>"}
 SQUARE_TRAFFIC_KEY = {"f32": "small_tma_f32_kernel", "f64": "small_fast_kernel<f64>",
-                      "c64": "small_fast_kernel<c64>", "c128": "small_fast_kernel<c128>"}
+                      "c64": "small_tma_c64_kernel", "c128": "small_fast_kernel<c128>"}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed launches
 FP64_PEAK_TFLOPS = 1.25          # nominal GB300 FP64 rate (DFMA and FP64 MMA alike); no measured figure
 # nominal dense tensor rates of one GB300 (TFLOP/s): their ratio scales the
