@@ -4,8 +4,8 @@
 // product is a thin matrix-vector product bound by reading L once from HBM,
 // and the per-block-row launches dominate.  This path keeps the blocked
 // algorithm of "Hierarchical Shared Memory-Aware Optimization for TRSM on GPU
-// Platforms" -- the diagonal blocks inverted up front (W_t = D_t^{-1}, the
-// same inversion kernels), then per block row t
+// Platforms" -- the diagonal blocks inverted up front (W_t = D_t^{-1}), then
+// per block row t
 //     x_t = W_t (alpha b_t - sum_{s<t} L_ts x_s)
 // -- but runs all block rows in one cooperatively launched persistent
 // kernel.  The CTA that owns block row t streams its tiles L_ts (s < t) and
@@ -25,8 +25,10 @@
 //             once per product in shared memory.  In f32 with n = 1 the
 //             tile on the chain, L_{t,t-1}, and W_t are moved to registers
 //             before x_{t-1} arrives.
+// In the cluster form (CL) consecutive block rows sit in a cluster and x_t
+// also goes straight into the next CTA's shared memory (see the kernel).
 // Every wait is bounded; on expiry the CTA records TRSM_ERR_DEVICE_TIMEOUT,
-// lets its copies in flight land and returns.
+// lets its copies and hand-offs in flight land and returns.
 #pragma once
 
 #include <type_traits>
