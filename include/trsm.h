@@ -261,9 +261,12 @@ int trsm_trtri_lower(trsm_dtype_t dtype, int64_t m, const void *A, int64_t lda,
  * the call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  m <= 64 needs no workspace.  For m > 64 the blocked path's
  * workspace lives in a fixed device array of TRSM_NOALLOC_SCRATCH_BYTES
- * inside the library; a problem whose workspace
- * (trsm_llnn_workspace_bytes(dtype, m, n, 0)) exceeds it is rejected with
- * TRSM_ERR_WORKSPACE before anything is launched.
+ * inside the library.  The block size is trsm_llnn's (the table's) when its
+ * workspace (trsm_llnn_workspace_bytes(dtype, m, n, 0)) fits the array,
+ * else the largest smaller one (256, 128) whose workspace fits -- the same
+ * solve with narrower blocks, so results agree with trsm_llnn to rounding;
+ * a problem that fits at none is rejected with TRSM_ERR_WORKSPACE before
+ * anything is launched.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that

@@ -117,7 +117,8 @@ SEQUENCES = {
 def test_noalloc_matches_allocating_entry_and_oracle_on_consecutive_calls(env, dtype):
     lib = env["lib"]
     for i, (m, n, alpha) in enumerate(SEQUENCES[dtype]):
-        need = lib.trsm_llnn_workspace_bytes(CODE[dtype], m, n, 0)
+        # the table's block size, else the largest smaller one, fits the array
+        need = min(lib.trsm_llnn_workspace_bytes(CODE[dtype], m, n, nb) for nb in (0, 256, 128))
         assert 0 < need <= SCRATCH_BYTES
         al = complex(alpha, 0.25) if ti.IS_COMPLEX[dtype] else alpha
         p = Problem(env, dtype, m, n, al, seed=40 + i)
@@ -164,7 +165,7 @@ def test_noalloc_rejects_problems_beyond_its_array(env):
     # exceed the 32 MiB array for every block size, so the call must be
     # rejected before anything is launched (the buffers below are tiny)
     m = n = 16384
-    need = env["lib"].trsm_llnn_workspace_bytes(CODE["c128"], m, n, 0)
+    need = min(env["lib"].trsm_llnn_workspace_bytes(CODE["c128"], m, n, nb) for nb in (0, 256, 128))
     assert need > SCRATCH_BYTES
     a = torch.zeros(1, dtype=torch.complex128, device="cuda")
     rc = env["lib"].trsm_llnn_noalloc(CODE["c128"], m, n, _alpha("c128", 1 + 0j), a.data_ptr(), m,

@@ -102,19 +102,25 @@ extern "C" int trsm_llnn_noalloc(trsm_dtype_t dtype, int64_t m, int64_t n, const
     if (!B || !aligned_to(B, eb)) return -7;
     if (m <= 64 && n > 64LL * 65535) return -3;
 
-    // Only the blocked path (m > 64) reads a workspace; its size with the
-    // table's block size decides up front whether the array can hold it.
+    // Only the blocked path (m > 64) reads a workspace; its size decides up
+    // front whether the array can hold it: with the table's block size, else
+    // with the largest smaller one that fits.
     void *scratch = nullptr;
+    int64_t nb_arg = 0;  // 0: the table's block size, as trsm_llnn
     if (m > 64 && !zero) {
-        const int nb = trsm_llnn_select_nb(dtype, m, n);
+        const int64_t table_nb = trsm_llnn_select_nb(dtype, m, n);
+        int64_t nb = table_nb;
+        while (nb > 128 && blocked_workspace_bytes((int)dtype, m, n, nb) > (size_t)TRSM_NOALLOC_SCRATCH_BYTES) nb /= 2;
         if (blocked_workspace_bytes((int)dtype, m, n, nb) > (size_t)TRSM_NOALLOC_SCRATCH_BYTES)
             return TRSM_ERR_WORKSPACE;
+        if (nb != table_nb) nb_arg = nb;
         const int rc = scratch_on_current_device(&scratch);
         if (rc != TRSM_SUCCESS) return rc;
     }
     // The same dispatch as trsm_llnn, with the array as the workspace and
-    // allocation switched off: both entry points pick the same kernels.
-    return solve_dispatch((int)dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, 0, scratch,
+    // allocation switched off: both entry points pick the same kernels
+    // whenever the table's block size fits.
+    return solve_dispatch((int)dtype, TRSM_COL_MAJOR, m, n, alpha, A, lda, 0, B, ldb, 0, 1, nb_arg, scratch,
                           scratch ? (size_t)TRSM_NOALLOC_SCRATCH_BYTES : 0, /*may_alloc=*/false,
                           static_cast<cudaStream_t>(stream), nullptr);
 }
